@@ -1,0 +1,492 @@
+// The extern "C" entry points of libsffn.so: argument checks, handles,
+// workspace layout and the order in which the kernels are enqueued.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "internal.h"
+
+namespace sffn {
+
+namespace {
+thread_local std::string g_last_error;
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int wbytes_of(int wdtype) { return wdtype == SFFN_F32 ? 4 : 2; }
+
+sffn_status invalid(const char* msg) {
+  set_error(msg);
+  return SFFN_ERR_INVALID_ARG;
+}
+
+// Column slicing of the down projection: as many slices (<= 16) as keep a
+// slice row chunk between 512 bytes and 4 KB and a multiple of 16 bytes.
+bool choose_down_shape(sffn_layer& L) {
+  const int d = L.desc.d, wb = L.wbytes;
+  for (int ns = 16; ns >= 1; ns >>= 1) {
+    if (d % ns) continue;
+    const int W = d / ns;
+    const int bytes = W * wb;
+    if (bytes % 16 || bytes > 4096) continue;
+    if (ns > 1 && bytes < 512) continue;
+    L.down_slices = ns;
+    L.down_width = W;
+    L.down_rows_per_stage = std::min(32, std::max(1, kDownStageBytes / bytes));
+    const int stage = L.down_rows_per_stage * bytes;
+    L.down_stages = std::min(8, std::max(2, kDownSmemBudget / stage));
+    return true;
+  }
+  return false;
+}
+
+sffn_status check_device(int want) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != want) return invalid("the current CUDA device is not the one the handle was created on");
+  return SFFN_OK;
+}
+
+sffn_status check_ws(const sffn_layer* L, int B, const void* ws, size_t ws_bytes) {
+  if (!ws) return invalid("ws is NULL");
+  if (!aligned(ws, 256)) return invalid("ws must be 256-byte aligned");
+  if (ws_bytes < ws_layout(*L, B).total) return invalid("ws_bytes is smaller than sffn_workspace_bytes(layer, B)");
+  return SFFN_OK;
+}
+
+sffn_status check_batch(const sffn_layer* L, int B) {
+  if (B < 1 || B > L->desc.max_batch) return invalid("B must be in [1, max_batch]");
+  if (B > 1) {
+    set_error("batch sizes above 1 are not implemented in this build");
+    return SFFN_ERR_UNSUPPORTED;
+  }
+  return SFFN_OK;
+}
+
+// Records the layer's trace event for kernel slot k (if any) around `launch`.
+template <typename F>
+cudaError_t traced(const sffn_layer& L, int k, cudaStream_t st, F&& launch) {
+  cudaError_t e = cudaSuccess;
+  if (L.trace_begin[k]) e = cudaEventRecord(L.trace_begin[k], st);
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess && L.trace_end[k]) e = cudaEventRecord(L.trace_end[k], st);
+  return e;
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+sffn_status cuda_fail(cudaError_t e, const char* what) {
+  char buf[512];
+  snprintf(buf, sizeof(buf), "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+  g_last_error = buf;
+  if (e == cudaErrorMemoryAllocation) return SFFN_ERR_OOM;
+  return SFFN_ERR_CUDA;
+}
+
+WsLayout ws_layout(const sffn_layer& L, int B) {
+  WsLayout w;
+  size_t off = 0;
+  w.hid = off;
+  off = align256(off + (size_t)B * L.desc.h * 4);
+  w.hval = off;
+  off = align256(off + (size_t)B * L.desc.f * 4);
+  w.alist = off;
+  off = align256(off + (size_t)B * L.desc.f * 4);
+  w.count = off;
+  off = align256(off + (size_t)(B + 1) * 4);
+  w.total = off;
+  return w;
+}
+
+}  // namespace sffn
+
+using namespace sffn;
+
+extern "C" {
+
+const char* sffn_status_string(sffn_status s) {
+  switch (s) {
+    case SFFN_OK: return "SFFN_OK";
+    case SFFN_ERR_INVALID_ARG: return "SFFN_ERR_INVALID_ARG";
+    case SFFN_ERR_UNSUPPORTED: return "SFFN_ERR_UNSUPPORTED";
+    case SFFN_ERR_CUDA: return "SFFN_ERR_CUDA";
+    case SFFN_ERR_TIMEOUT: return "SFFN_ERR_TIMEOUT";
+    case SFFN_ERR_OOM: return "SFFN_ERR_OOM";
+    case SFFN_ERR_DEVICE: return "SFFN_ERR_DEVICE";
+  }
+  return "SFFN_ERR_UNKNOWN";
+}
+
+const char* sffn_last_error(void) { return g_last_error.c_str(); }
+
+const char* sffn_version(void) { return "sffn 0.1 sm_103a"; }
+
+sffn_status sffn_layer_validate(const sffn_layer_desc* desc) {
+  if (!desc) return invalid("desc is NULL");
+  const sffn_layer_desc& D = *desc;
+  if (D.wdtype != SFFN_F32 && D.wdtype != SFFN_F16 && D.wdtype != SFFN_BF16) return invalid("wdtype is not an sffn_dtype");
+  if (D.act != SFFN_ACT_RELU && D.act != SFFN_ACT_REGLU && D.act != SFFN_ACT_SWIGLU) return invalid("act is not an sffn_act");
+  if (D.d < 8 || D.d > 16384 || D.d % 8) return invalid("d must be a multiple of 8 in [8, 16384]");
+  if ((long long)D.d * wbytes_of(D.wdtype) > 32768) return invalid("a weight row (d * element size) must be at most 32 KB");
+  if (D.h < 8 || D.h > 4096 || D.h % 8) return invalid("h must be a multiple of 8 in [8, 4096]");
+  if (D.group_size != 32 && D.group_size != 64) return invalid("group_size must be 32 or 64");
+  if (D.f < D.group_size || D.f % D.group_size) return invalid("f must be a positive multiple of group_size");
+  if (D.f / D.group_size > 1024) return invalid("at most 1024 groups per layer");
+  if (D.max_batch < 1 || D.max_batch > 32) return invalid("max_batch must be in [1, 32]");
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
+  if (!out) return invalid("out is NULL");
+  sffn_status rc = sffn_layer_validate(desc);
+  if (rc != SFFN_OK) return rc;
+  sffn_layer* L = new (std::nothrow) sffn_layer();
+  if (!L) return invalid("host allocation failed");
+  L->desc = *desc;
+  L->wbytes = wbytes_of(desc->wdtype);
+  L->n_groups = desc->f / desc->group_size;
+  L->nwords = desc->f / 32;
+  L->gwords = (L->n_groups + 31) / 32;
+  if (!choose_down_shape(*L)) {
+    delete L;
+    set_error("no column slicing of d fits the down-projection kernel");
+    return SFFN_ERR_UNSUPPORTED;
+  }
+  {
+    const size_t stage = (size_t)desc->d * L->wbytes * (desc->act == SFFN_ACT_RELU ? 1 : 2);
+    L->up_stages = (int)std::min<size_t>(8, std::max<size_t>(2, kUpSmemBudget / stage));
+  }
+  cudaError_t e = cudaGetDevice(&L->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail(e, "sffn_layer_create: device query");
+  }
+  const size_t d = desc->d, f = desc->f, h = desc->h, wb = L->wbytes;
+  struct {
+    void** p;
+    size_t bytes;
+  } allocs[] = {
+      {&L->W1, h * d * wb},
+      {(void**)&L->b1, h * 4},
+      {&L->W2, f * h * wb},
+      {(void**)&L->b2, f * 4},
+      {&L->up, f * d * wb},
+      {&L->gate, desc->act == SFFN_ACT_RELU ? 0 : f * d * wb},
+      {&L->downT, f * d * wb},
+      {(void**)&L->perm, f * 4},
+      {(void**)&L->err, 256},
+  };
+  for (auto& a : allocs) {
+    if (!a.bytes) continue;
+    e = cudaMalloc(a.p, a.bytes);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(e, "sffn_layer_create: cudaMalloc");
+      sffn_layer_destroy(L);
+      return rc;
+    }
+  }
+  e = cudaMemset(L->err, 0, 256);
+  if (e == cudaSuccess) e = configure_kernels(*L);
+  if (e != cudaSuccess) {
+    rc = cuda_fail(e, "sffn_layer_create: kernel set-up");
+    sffn_layer_destroy(L);
+    return rc;
+  }
+  *out = L;
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_pack(sffn_layer* L, const void* W1, const float* b1, const void* W2, const float* b2,
+                            const void* up, const void* gate, const void* down, const int32_t* perm,
+                            sffn_stream stream) {
+  if (!L) return invalid("layer is NULL");
+  if (!W1 || !W2 || !up || !down) return invalid("W1, W2, up and down are required");
+  if (L->desc.act != SFFN_ACT_RELU && !gate) return invalid("gate is required for ReGLU and SwiGLU");
+  const void* ptrs[] = {W1, W2, up, down, gate, b1, b2, perm};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return invalid("weight, bias and perm pointers must be 16-byte aligned");
+  sffn_status rc = check_device(L->device);
+  if (rc != SFFN_OK) return rc;
+  return pack_layer(*L, W1, b1, W2, b2, up, L->desc.act == SFFN_ACT_RELU ? nullptr : gate, down, perm,
+                    (cudaStream_t)stream);
+}
+
+sffn_status sffn_layer_get_desc(const sffn_layer* L, sffn_layer_desc* out) {
+  if (!L || !out) return invalid("layer or out is NULL");
+  *out = L->desc;
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_packed(const sffn_layer* L, sffn_packed_view* out) {
+  if (!L || !out) return invalid("layer or out is NULL");
+  out->W1 = L->W1;
+  out->b1 = L->b1;
+  out->W2 = L->W2;
+  out->b2 = L->b2;
+  out->up = L->up;
+  out->gate = L->gate;
+  out->downT = L->downT;
+  out->perm = L->perm;
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_set_trace(sffn_layer* L, const sffn_trace* t) {
+  if (!L) return invalid("layer is NULL");
+  for (int k = 0; k < 4; ++k) {
+    L->trace_begin[k] = t ? static_cast<cudaEvent_t>(t->begin[k]) : nullptr;
+    L->trace_end[k] = t ? static_cast<cudaEvent_t>(t->end[k]) : nullptr;
+  }
+  return SFFN_OK;
+}
+
+size_t sffn_workspace_bytes(const sffn_layer* L, int32_t B) {
+  if (!L || B < 1 || B > L->desc.max_batch) return 0;
+  return ws_layout(*L, B).total;
+}
+
+static sffn_status read_error_word(uint32_t* err, cudaStream_t st) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "check_error: synchronize");
+  uint32_t h = 0;
+  e = cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h) e = cudaMemset(err, 0, 4);
+  if (e != cudaSuccess) return cuda_fail(e, "check_error: read error word");
+  if (h == SFFN_ERR_TIMEOUT) {
+    set_error("a bounded device-side wait ran out");
+    return SFFN_ERR_TIMEOUT;
+  }
+  if (h) {
+    set_error("the device flagged bad data");
+    return SFFN_ERR_DEVICE;
+  }
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_check_error(const sffn_layer* L, sffn_stream stream) {
+  if (!L) return invalid("layer is NULL");
+  return read_error_word(L->err, (cudaStream_t)stream);
+}
+
+void sffn_layer_destroy(sffn_layer* L) {
+  if (!L) return;
+  void* ps[] = {L->W1, L->b1, L->W2, L->b2, L->up, L->gate, L->downT, L->perm, L->err};
+  for (void* p : ps)
+    if (p) cudaFree(p);
+  delete L;
+}
+
+// ---------------------------------------------------------------- hot calls
+
+static sffn_status check_hot(const sffn_layer* L, const float* x, int B, const sffn_masks* m, const void* ws,
+                             size_t ws_bytes) {
+  if (!L) return invalid("layer is NULL");
+  if (!x || !aligned(x, 16)) return invalid("x must be a non-NULL 16-byte aligned device pointer");
+  if (!m || !m->nmask) return invalid("masks and masks->nmask are required");
+  sffn_status rc = check_batch(L, B);
+  if (rc != SFFN_OK) return rc;
+  rc = check_ws(L, B, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  return check_device(L->device);
+}
+
+sffn_status sffn_predict(const sffn_layer* L, const float* x, int32_t B, float thres, const sffn_masks* m, void* ws,
+                         size_t ws_bytes, sffn_stream stream) {
+  sffn_status rc = check_hot(L, x, B, m, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = ws_layout(*L, B);
+  float* hid = reinterpret_cast<float*>(static_cast<char*>(ws) + w.hid);
+  cudaError_t e = traced(*L, 0, st, [&] { return launch_pred_hidden(*L, x, hid, st); });
+  if (e == cudaSuccess) e = traced(*L, 1, st, [&] { return launch_pred_scores(*L, hid, thres, m->nmask, st); });
+  if (e == cudaSuccess && (m->idx || m->count || m->gmask))
+    e = launch_mask_views(*L, m->nmask, m->idx, m->count, m->gmask, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_predict: launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const sffn_masks* m, float* y,
+                         float* x_out, void* ws, size_t ws_bytes, sffn_stream stream) {
+  sffn_status rc = check_hot(L, x, B, m, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  if (!y || !aligned(y, 16)) return invalid("y must be a non-NULL 16-byte aligned device pointer");
+  if (y == x) return invalid("y must not alias x");
+  if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = ws_layout(*L, B);
+  char* base = static_cast<char*>(ws);
+  float* hval = reinterpret_cast<float*>(base + w.hval);
+  int32_t* alist = reinterpret_cast<int32_t*>(base + w.alist);
+  int32_t* cnt = reinterpret_cast<int32_t*>(base + w.count);
+  cudaError_t e = traced(*L, 2, st, [&] {
+    return launch_gather_up(*L, x, m->nmask, nullptr, nullptr, nullptr, hval, alist, cnt, st);
+  });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_down(*L, hval, alist, cnt, x, y, x_out, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_forward: launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, float thres, const sffn_masks* m,
+                             float* y, float* x_out, void* ws, size_t ws_bytes, sffn_stream stream) {
+  sffn_status rc = check_hot(L, x, B, m, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  if (!y || !aligned(y, 16)) return invalid("y must be a non-NULL 16-byte aligned device pointer");
+  if (y == x) return invalid("y must not alias x");
+  if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = ws_layout(*L, B);
+  char* base = static_cast<char*>(ws);
+  float* hid = reinterpret_cast<float*>(base + w.hid);
+  float* hval = reinterpret_cast<float*>(base + w.hval);
+  int32_t* alist = reinterpret_cast<int32_t*>(base + w.alist);
+  int32_t* cnt = reinterpret_cast<int32_t*>(base + w.count);
+  cudaError_t e = traced(*L, 0, st, [&] { return launch_pred_hidden(*L, x, hid, st); });
+  if (e == cudaSuccess) e = traced(*L, 1, st, [&] { return launch_pred_scores(*L, hid, thres, m->nmask, st); });
+  if (e == cudaSuccess)
+    e = traced(*L, 2, st, [&] {
+      return launch_gather_up(*L, x, m->nmask, m->idx, m->count, m->gmask, hval, alist, cnt, st);
+    });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_down(*L, hval, alist, cnt, x, y, x_out, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
+  return SFFN_OK;
+}
+
+// ---------------------------------------------------------------- TAM
+
+sffn_status tam_create(int32_t n_layers, int32_t n_groups, float lambda0, tam_state** out) {
+  if (!out) return invalid("out is NULL");
+  if (n_layers < 1 || n_layers > 4096) return invalid("n_layers must be in [1, 4096]");
+  if (n_groups < 1 || n_groups > 1024) return invalid("n_groups must be in [1, 1024]");
+  if (!(lambda0 > 0.f && lambda0 < 1.f)) return invalid("lambda0 must be in (0, 1)");
+  tam_state* S = new (std::nothrow) tam_state();
+  if (!S) return invalid("host allocation failed");
+  S->n_layers = n_layers;
+  S->n_groups = n_groups;
+  S->gwords = (n_groups + 31) / 32;
+  cudaError_t e = cudaGetDevice(&S->device);
+  if (e == cudaSuccess) e = cudaMalloc(&S->scores, (size_t)n_layers * n_groups * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&S->lambdas, (size_t)n_layers * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&S->resident, (size_t)n_layers * S->gwords * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&S->err, 256);
+  if (e == cudaSuccess) e = cudaMemset(S->scores, 0, (size_t)n_layers * n_groups * 4);
+  if (e == cudaSuccess) e = cudaMemset(S->resident, 0, (size_t)n_layers * S->gwords * 4);
+  if (e == cudaSuccess) e = cudaMemset(S->err, 0, 256);
+  if (e == cudaSuccess) {
+    float* h = new (std::nothrow) float[n_layers];
+    if (!h) {
+      tam_destroy(S);
+      return invalid("host allocation failed");
+    }
+    for (int i = 0; i < n_layers; ++i) h[i] = lambda0;
+    e = cudaMemcpy(S->lambdas, h, (size_t)n_layers * 4, cudaMemcpyHostToDevice);
+    delete[] h;
+  }
+  if (e != cudaSuccess) {
+    sffn_status rc = cuda_fail(e, "tam_create");
+    tam_destroy(S);
+    return rc;
+  }
+  *out = S;
+  return SFFN_OK;
+}
+
+sffn_status tam_update(tam_state* S, int32_t layer0, int32_t n_layers, const uint32_t* gmask, int32_t gstride,
+                       float lambda, float eps, int32_t K, const tam_outputs* out, sffn_stream stream) {
+  if (!S) return invalid("tam is NULL");
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > S->n_layers) return invalid("layer range out of bounds");
+  if (!gmask || !aligned(gmask, 4)) return invalid("gmask must be a non-NULL 4-byte aligned device pointer");
+  if (gstride < S->gwords) return invalid("gmask_stride is shorter than a group bitset");
+  if (!(lambda < 1.f) || std::isnan(lambda)) return invalid("lambda must be < 1 (negative: use the state's lambda)");
+  if (!(eps >= 0.f) || std::isinf(eps)) return invalid("eps must be finite and >= 0");
+  if (K < 0 || K > S->n_groups) return invalid("capacity_k must be in [0, n_groups]");
+  sffn_status rc = check_device(S->device);
+  if (rc != SFFN_OK) return rc;
+  tam_outputs o = {};
+  if (out) o = *out;
+  cudaError_t e = launch_tam_update(*S, layer0, n_layers, gmask, gstride, lambda, eps, K, o, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tam_update: launch");
+  return SFFN_OK;
+}
+
+sffn_status tam_adapt(tam_state* S, int32_t layer0, int32_t n_layers, const uint8_t* stall, float alpha, float lo,
+                      float hi, sffn_stream stream) {
+  if (!S) return invalid("tam is NULL");
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > S->n_layers) return invalid("layer range out of bounds");
+  if (!stall) return invalid("stall is NULL");
+  if (!(alpha >= 0.f) || std::isinf(alpha)) return invalid("alpha must be finite and >= 0");
+  if (!(lo > 0.f && lo <= hi && hi < 1.f)) return invalid("need 0 < lo <= hi < 1");
+  sffn_status rc = check_device(S->device);
+  if (rc != SFFN_OK) return rc;
+  cudaError_t e = launch_tam_adapt(*S, layer0, n_layers, stall, alpha, lo, hi, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tam_adapt: launch");
+  return SFFN_OK;
+}
+
+sffn_status tam_get_state(const tam_state* S, float* scores, float* lambdas, uint32_t* resident, sffn_stream stream) {
+  if (!S) return invalid("tam is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  if (scores) e = cudaMemcpyAsync(scores, S->scores, (size_t)S->n_layers * S->n_groups * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && lambdas)
+    e = cudaMemcpyAsync(lambdas, S->lambdas, (size_t)S->n_layers * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && resident)
+    e = cudaMemcpyAsync(resident, S->resident, (size_t)S->n_layers * S->gwords * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "tam_get_state");
+  return SFFN_OK;
+}
+
+sffn_status tam_set_state(tam_state* S, const float* scores, const float* lambdas, const uint32_t* resident,
+                          sffn_stream stream) {
+  if (!S) return invalid("tam is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaSuccess;
+  if (scores) e = cudaMemcpyAsync(S->scores, scores, (size_t)S->n_layers * S->n_groups * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && lambdas)
+    e = cudaMemcpyAsync(S->lambdas, lambdas, (size_t)S->n_layers * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && resident)
+    e = cudaMemcpyAsync(S->resident, resident, (size_t)S->n_layers * S->gwords * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "tam_set_state");
+  return SFFN_OK;
+}
+
+sffn_status tam_get_shape(const tam_state* S, int32_t* n_layers, int32_t* n_groups) {
+  if (!S || !n_layers || !n_groups) return invalid("tam, n_layers or n_groups is NULL");
+  *n_layers = S->n_layers;
+  *n_groups = S->n_groups;
+  return SFFN_OK;
+}
+
+sffn_status tam_check_error(const tam_state* S, sffn_stream stream) {
+  if (!S) return invalid("tam is NULL");
+  return read_error_word(S->err, (cudaStream_t)stream);
+}
+
+void tam_destroy(tam_state* S) {
+  if (!S) return;
+  void* ps[] = {S->scores, S->lambdas, S->resident, S->err};
+  for (void* p : ps)
+    if (p) cudaFree(p);
+  delete S;
+}
+
+// ---------------------------------------------------------------- self-test
+
+sffn_status sffn_selftest_wait_timeout(const sffn_layer* L, int32_t limit_us, sffn_stream stream) {
+  if (!L) return invalid("layer is NULL");
+  if (limit_us < 1 || limit_us > 100000) return invalid("limit_us must be in [1, 100000]");
+  sffn_status rc = check_device(L->device);
+  if (rc != SFFN_OK) return rc;
+  cudaError_t e = launch_selftest_timeout(L->err, limit_us, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_selftest_wait_timeout: launch");
+  return SFFN_OK;
+}
+
+}  // extern "C"

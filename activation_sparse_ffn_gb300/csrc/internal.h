@@ -1,0 +1,139 @@
+// Host-side internals of libsffn: the layer and momentum-state handles, the
+// workspace layout, and the per-kernel launchers implemented in the .cu files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "sffn.h"
+
+struct sffn_layer {
+  sffn_layer_desc desc;
+  int device = 0;
+  int num_sms = 0;
+  int wbytes = 0;       // bytes per stored weight
+  int n_groups = 0;
+  int nwords = 0;       // f / 32
+  int gwords = 0;       // ceil(n_groups / 32)
+  void* W1 = nullptr;
+  float* b1 = nullptr;
+  void* W2 = nullptr;
+  float* b2 = nullptr;
+  void* up = nullptr;
+  void* gate = nullptr;
+  void* downT = nullptr;
+  int32_t* perm = nullptr;
+  uint32_t* err = nullptr;  // device error word
+  bool has_b1 = false, has_b2 = false;
+  // launch shapes chosen at create time
+  int up_stages = 0;        // gather-up ring depth
+  int down_slices = 0;      // column slices of the down projection
+  int down_width = 0;       // columns per slice
+  int down_rows_per_stage = 0;
+  int down_stages = 0;
+  // optional timing hooks (sffn_layer_set_trace)
+  cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+
+struct tam_state {
+  int n_layers = 0;
+  int n_groups = 0;
+  int gwords = 0;
+  int device = 0;
+  float* scores = nullptr;     // [L][n_groups]
+  float* lambdas = nullptr;    // [L]
+  uint32_t* resident = nullptr;  // [L][gwords]
+  uint32_t* err = nullptr;
+};
+
+namespace sffn {
+
+constexpr int kClusterSplit = 8;     // thread blocks per cluster in the down projection
+constexpr int kUpSmemBudget = 128 * 1024;
+constexpr int kDownStageBytes = 16 * 1024;
+constexpr int kDownSmemBudget = 80 * 1024;
+
+// Shared memory of the down projection: one region used first as the row
+// ring and then for the per-block column partials ([rows lanes][W] + [W]
+// floats), followed by the stage barriers.
+__host__ __device__ inline size_t down_region_bytes(int W, int wbytes, int rows_per_stage, int stages, int threads) {
+  const size_t ring = (size_t)stages * rows_per_stage * W * wbytes;
+  const int cpr = W * wbytes / 16;
+  const size_t red = ((size_t)(threads / cpr) * W + W) * 4;
+  const size_t r = ring > red ? ring : red;
+  return (r + 15) & ~(size_t)15;
+}
+
+// Workspace of one hot call for batch size B (offsets in bytes, 256-aligned).
+struct WsLayout {
+  size_t hid = 0;     // float [B][h]
+  size_t hval = 0;    // float [B][f]: activation values in active-list order
+  size_t alist = 0;   // int32 [B][f]: active slots, ascending
+  size_t count = 0;   // int32 [B] (+ padding)
+  size_t total = 0;
+};
+WsLayout ws_layout(const sffn_layer& L, int B);
+
+void set_error(const std::string& msg);
+sffn_status cuda_fail(cudaError_t e, const char* what);
+
+// Launchers (each enqueues kernels on `st`; they return the launch status).
+cudaError_t launch_pred_hidden(const sffn_layer& L, const float* x, float* hid, cudaStream_t st);
+cudaError_t launch_pred_scores(const sffn_layer& L, const float* hid, float thres, uint32_t* nmask,
+                               cudaStream_t st);
+cudaError_t launch_mask_views(const sffn_layer& L, const uint32_t* nmask, int32_t* idx, int32_t* count,
+                              uint32_t* gmask, cudaStream_t st);
+cudaError_t launch_gather_up(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
+                             int32_t* count_out, uint32_t* gmask_out, float* hval, int32_t* alist,
+                             int32_t* ws_count, cudaStream_t st);
+cudaError_t launch_down(const sffn_layer& L, const float* hval, const int32_t* alist, const int32_t* ws_count,
+                        const float* x, float* y, float* x_out, cudaStream_t st);
+cudaError_t launch_tam_update(tam_state& S, int layer0, int n_layers, const uint32_t* gmask, int gstride,
+                              float lambda, float eps, int K, const tam_outputs& out, cudaStream_t st);
+cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8_t* stall, float alpha,
+                             float lo, float hi, cudaStream_t st);
+cudaError_t launch_selftest_timeout(uint32_t* err, int limit_us, cudaStream_t st);
+
+// Packing (setup).
+sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const void* W2, const float* b2,
+                       const void* up, const void* gate, const void* down, const int32_t* perm,
+                       cudaStream_t st);
+
+// Shared memory sizes, set as kernel attributes at layer creation.
+cudaError_t configure_kernels(sffn_layer& L);
+size_t gather_up_smem(const sffn_layer& L);
+size_t down_smem(const sffn_layer& L);
+
+// Launch helper: programmatic dependent launch and optional cluster size.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      bool pdl, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+}  // namespace sffn

@@ -1,0 +1,515 @@
+#!/usr/bin/env python3
+"""Throughput of the activation-sparse FFN decode step on GB300.
+
+One step = one decode token through every layer of the workload's stack:
+per layer the predictor (hidden + scores/threshold/ballot), the gather of
+active up/gate rows with the fused activation, the down projection with the
+residual add, then one momentum (TAM) update for all layers (and, for the
+adaptive-lambda workload, one balancer step). Inputs are seeded synthetic
+layers and token sequences resident in HBM before timing starts; every step
+touches more distinct weight bytes than L2 holds.
+
+Output: one JSON line (rank 0). Multi-GPU runs are independent replicas
+(launch with torchrun); value = all ranks' tokens / max elapsed.
+
+  python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llama2_70b_reglu_d8192_f28672_bf16_8l"
+METRIC = "sparse-FFN decode tokens/s at B=1; active-byte HBM GB/s as % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS = ("pred_hidden", "pred_scores", "gather_up", "down")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--tokens", type=int, default=128, help="distinct tokens cycled through (one graph each)")
+    p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
+    p.add_argument("--profile-steps", type=int, default=64)
+    p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-max-steps", type=int, default=24)
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 11:
+                    rows.append(parts)
+        os.unlink(self.path)
+        busy = [r for r in rows if _num(r[5]) is not None and _num(r[5]) >= 50] or rows
+        sm = [_num(r[2]) for r in busy if _num(r[2]) is not None]
+        smax = [_num(r[3]) for r in rows if _num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[7 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(busy),
+                "power_w_max": max((_num(r[4]) or 0) for r in busy) if busy else None}
+
+
+def _num(s):
+    try:
+        return float(s)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def layer_bytes(spec, count: int, with_b2: bool) -> dict:
+    """Algorithmic bytes of one layer-token, per kernel: the weight rows the
+    method must read plus the small vectors each kernel must move."""
+    d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
+    nmat_up = 1 if spec.act == "relu" else 2
+    k = {
+        "pred_hidden": h * d * wb + d * 4 + h * 4,
+        "pred_scores": f * h * wb + h * 4 + f // 8 + (f * 4 if with_b2 else 0),
+        "gather_up": count * nmat_up * d * wb + d * 4 + f // 8 + count * 8,
+        "down": count * d * wb + count * 8 + 3 * d * 4,
+    }
+    # the metric: predictor weights + all rows of active neurons + x + y
+    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + count * spec.n_mats * d * wb + 2 * d * 4
+    return {"kernels": k, "metric": metric}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        if rank == 0:
+            __graft_entry__.build()
+        dist.barrier()
+    else:
+        torch.cuda.set_device(local)
+        __graft_entry__.build()
+    from activation_sparse_ffn_gb300 import sffn
+    from activation_sparse_ffn_gb300 import workload as W
+
+    spec = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    nL = spec.layers
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+
+    # ---- layers (generated on the device, packed, originals freed)
+    layers, host0 = [], None
+    with torch.cuda.stream(stream):
+        for l in range(nL):
+            w = W.make_layer(spec, seed=args.seed, layer=l, device=dev)
+            layers.append(sffn.Layer.from_weights(w, spec.group_size, spec.act, max_batch=1, stream=stream))
+            if l == 0 and want_cpu:
+                host0 = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v)
+                         for k, v in w.items()}
+                host0["perm"] = w["perm"].cpu().numpy()
+                host0["b2f"] = None if w["b2"] is None else w["b2"].double().cpu().numpy()
+            del w
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    with_b2 = spec.bias_mode
+
+    # ---- buffers
+    P = max(1, min(args.tokens, spec.tokens))
+    X = W.make_tokens(spec.d, P, seed=args.seed, kind=spec.seq, device=dev).contiguous()  # [P,1,d]
+    gw = (spec.n_groups + 31) // 32
+    gmask_all = torch.zeros(nL, gw, dtype=torch.int32, device=dev)
+    masks = []
+    for l in range(nL):
+        m = layers[l].masks(1, device=dev)
+        m.c.gmask = gmask_all[l].data_ptr()
+        masks.append(m)
+    ws = layers[0].workspace(1, device=dev)
+    xa = torch.empty(1, spec.d, device=dev)
+    xb = torch.empty(1, spec.d, device=dev)
+    ybuf = torch.empty(1, spec.d, device=dev)
+    tam = sffn.Tam(nL, spec.n_groups, spec.tam_lambda)
+    K = spec.capacity
+    outs = sffn.TamOutputs(nL, spec.n_groups, K, device=dev)
+    stalls = torch.from_numpy(W.make_stall_bits(P, nL, seed=args.seed)).to(dev) if spec.anb else None
+    launches_per_step = nL * 4 + 1 + (1 if spec.anb else 0)
+
+    def step(t, xin=None):
+        x = X[t % P] if xin is None else xin
+        outb = (xa, xb)
+        for l in range(nL):
+            xo = outb[l % 2]
+            sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
+            x = xo
+        sffn.tam_update(tam.handle, 0, nL, gmask_all, gw, -1.0, spec.tam_eps, K, outs, stream)
+        if spec.anb:
+            sffn.tam_adapt(tam.handle, 0, nL, stalls[t % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, stream)
+        return x
+
+    # ---- census: active counts per (token, layer); deterministic given the token
+    counts = np.zeros((P, nL), dtype=np.int64)
+    with torch.cuda.stream(stream):
+        for t in range(P):
+            step(t)
+            counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
+    for L in layers:
+        L.check_error(stream)
+    metric_bytes = np.array([[layer_bytes(spec, int(counts[t, l]), with_b2)["metric"] for l in range(nL)]
+                             for t in range(P)]).sum(axis=1)
+
+    # ---- graphs: one per distinct token
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        with torch.cuda.stream(stream):
+            for t in range(P):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step(t)
+                graphs.append(g)
+        torch.cuda.synchronize()
+
+    def run(t):
+        if graphs is not None:
+            graphs[t % P].replay()
+        else:
+            step(t)
+
+    # ---- warm-up, then the timed region
+    with torch.cuda.stream(stream):
+        for t in range(args.warmup):
+            run(t)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_start = args.warmup
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            run(t_start + i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    for L in layers:
+        L.check_error(stream)
+    sffn.tam_check_error(tam.handle, stream)
+    toks = [(t_start + i) % P for i in range(args.steps)]
+    timed_bytes = float(sum(metric_bytes[t] for t in toks))
+    sec = elapsed_ms / 1e3
+    value = world * args.steps / sec
+    ms_per_step = elapsed_ms / args.steps
+    step_gbs = timed_bytes / sec / 1e9
+
+    # ---- traced pass: per-kernel durations (events around each kernel)
+    R = min(args.profile_steps, P)
+    ev = {k: [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
+              for _ in range(R)] for k in KERNELS}
+    tam_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            x = X[r % P]
+            outb = (xa, xb)
+            for l in range(nL):
+                sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KERNELS],
+                                          [ev[k][r][l][1] for k in KERNELS])
+                xo = outb[l % 2]
+                sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
+                x = xo
+            tam_ev[r][0].record(stream)
+            sffn.tam_update(tam.handle, 0, nL, gmask_all, gw, -1.0, spec.tam_eps, K, outs, stream)
+            tam_ev[r][1].record(stream)
+    torch.cuda.synchronize()
+    for L in layers:
+        sffn.sffn_layer_set_trace(L.handle)
+    per_kernel = {}
+    for k in KERNELS:
+        durs = [ev[k][r][l][0].elapsed_time(ev[k][r][l][1]) for r in range(R) for l in range(nL)]
+        kb = [layer_bytes(spec, int(counts[r % P, l]), with_b2)["kernels"][k] for r in range(R) for l in range(nL)]
+        per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
+                         "gbs": sum(kb) / (sum(durs) / 1e3) / 1e9}
+    tam_us = 1e3 * sum(a.elapsed_time(b) for a, b in tam_ev) / R
+    dom = max(KERNELS, key=lambda k: per_kernel[k]["us"])
+
+    # ---- dense run of the same layer: every neuron active (thres = -inf)
+    dense_us = None
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            sffn.sffn_decode_step(layers[0].handle, X[i % P], 1, float("-inf"), masks[0], ybuf, xa, ws, stream)
+        e0.record(stream)
+        nd = 20
+        for i in range(nd):
+            sffn.sffn_decode_step(layers[i % nL].handle, X[i % P], 1, float("-inf"), masks[i % nL], ybuf, xa, ws,
+                                  stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dense_us = 1e3 * e0.elapsed_time(e1) / nd
+
+    # ---- end to end through the public API with host buffers
+    Xh = X.cpu().pin_memory()
+    xin = torch.empty(1, spec.d, device=dev)
+    yh = torch.empty(1, spec.d).pin_memory()
+    g_e2e = None
+    if graphs is not None:
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g_e2e, stream=stream):
+                xfin = step(0, xin=xin)
+    E = min(args.e2e_steps, args.steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(E):
+            t = (t_start + i) % P
+            xin.copy_(Xh[t], non_blocking=True)
+            if g_e2e is not None:
+                g_e2e.replay()
+                out = xfin
+            else:
+                out = step(t, xin=xin)
+            yh.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_sec = time.perf_counter() - t0
+    e2e_value = world * E / e2e_sec
+
+    # ---- CPU baseline: the oracle on layer 0, as it stands
+    cpu = None
+    if want_cpu and host0 is not None:
+        cpu = cpu_baseline(spec, host0, X[:, 0].double().cpu().numpy(), args.cpu_seconds)
+
+    peak, peak_kind = measured_peaks()
+    pk = per_kernel[dom]
+    dom_traffic = None
+    active_frac = float(counts.mean() / spec.f)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": nL, "batch": 1,
+            "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype, "thres": spec.thres,
+            "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
+            "distinct_tokens": P, "graphs": graphs is not None,
+            "l2": "inputs larger than L2: each step reads %.2f GB of distinct weights" % (timed_bytes / args.steps / 1e9),
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "us_per_layer": round(1e3 * ms_per_step / nL, 3),
+        "active_frac": round(active_frac, 5),
+        "algorithmic_gbs": round(step_gbs, 1),
+        "algorithmic_hbm_frac": round(step_gbs / peak, 4),
+        "dense_us_per_layer": round(dense_us, 3),
+        "dense_speedup": round(dense_us / (1e3 * ms_per_step / nL), 3),
+        "kernels_us": {k: round(v["us"], 3) for k, v in per_kernel.items()} | {"tam_all_layers": round(tam_us, 3)},
+        "kernels_gbs": {k: round(v["gbs"], 1) for k, v in per_kernel.items()},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(pk["gbs"], 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(pk["gbs"] / peak, 4), "traffic": dom_traffic,
+                     "peak_kind": peak_kind},
+        "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": spec.d * 4,
+                "d2h_bytes_per_step": spec.d * 4, "steps": E, "sync_per_step": True},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(spec, host, Xs, seconds):
+    """The oracle as it stands on layer 0 of the stack, token after token,
+    for about ``seconds``; tokens/s of the whole stack = 1 / (layers x time
+    per layer-token)."""
+    import numpy as np
+    from oracle import sffn_oracle as O
+
+    W1 = O.widen(host["W1"], spec.wdtype)
+    W2 = O.widen(host["W2"], spec.wdtype)
+    perm = host["perm"]
+    times = []
+    t_end = time.perf_counter() + seconds
+    t = 0
+    while (time.perf_counter() < t_end or len(times) < 2) and len(times) < 10000:
+        x = Xs[t % Xs.shape[0]]
+        t0 = time.perf_counter()
+        s = O.predictor_scores(W2, O.predictor_hidden(W1, x), host.get("b2f"))[perm]
+        a = O.active_from_scores(s, spec.thres)
+        O.mask_views(a, spec.group_size)
+        O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, a, perm)
+        times.append(time.perf_counter() - t0)
+        t += 1
+    per_layer = sum(times) / len(times)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(1.0 / (spec.layers * per_layer), 4), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"layer 0 of {spec.layers}, {len(times)} tokens, {per_layer * 1e3:.1f} ms per layer-token "
+                      f"(numpy fp64, BLAS threads = available cores), stack time = {spec.layers} x layer time"}
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from activation_sparse_ffn_gb300 import workload as W
+    from oracle import sffn_oracle as O
+
+    spec = W.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = W.make_layer(spec, seed=args.seed, layer=0, device=dev)
+    host = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v) for k, v in w.items()}
+    perm = w["perm"].cpu().numpy()
+    b2 = None if w["b2"] is None else w["b2"].double().cpu().numpy()
+    del w
+    X = W.make_tokens(spec.d, max(1, min(args.tokens, spec.tokens)), seed=args.seed, kind=spec.seq)[:, 0]
+    Xs = X.double().numpy()
+    W1 = O.widen(host["W1"], spec.wdtype)
+    W2 = O.widen(host["W2"], spec.wdtype)
+
+    def one(t):
+        x = Xs[t % Xs.shape[0]]
+        s = O.predictor_scores(W2, O.predictor_hidden(W1, x), b2)[perm]
+        a = O.active_from_scores(s, spec.thres)
+        O.mask_views(a, spec.group_size)
+        O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, a, perm)
+
+    K = max(1, min(args.steps, args.ref_max_steps))
+    Wm = min(args.warmup, 2)
+    for t in range(Wm):
+        one(t)
+    t0 = time.perf_counter()
+    for i in range(K):
+        one(Wm + i)
+    sec = time.perf_counter() - t0
+    per_layer = sec / K
+    value = 1.0 / (spec.layers * per_layer)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"each step = the oracle on one layer-token (layer 0 of {spec.layers}); {K} steps "
+              f"(requested {args.steps}); stack time = {spec.layers} x layer time")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(1e3 * per_layer * spec.layers, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": spec.layers, "batch": 1},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+/*
+ * sffn.h -- C ABI of libsffn.so: predictor-gated, activation-sparse FFN decode
+ * on one GB300 (sm_103a), with group momentum (TAM) bookkeeping.
+ *
+ * Sources of the operations (page title, section):
+ *   PowerInfer (SOSP'24) summary page -- §5.1 per-layer MLP predictor
+ *     scores = W2 . ReLU(W1 . x); "Paper vs code": a neuron is computed iff
+ *     score >= threshold (default 0.0); §5.2 neuron table mapping packed slots
+ *     to the original matrix order; §5.3-§5.4 neuron-aware operators that
+ *     touch only active rows (up/gate) and columns (down), each thread block on
+ *     a disjoint neuron set; activation note: ReLU, ReGLU, SiLU-family.
+ *   KAIROX (OSDI'26) review page -- 核心方法 item 1/3: co-activation groups
+ *     stored as contiguous regions, at most 1024 groups per layer; item 4:
+ *     temporal activation momentum (TAM), candidates above
+ *     tau = (1 - lambda) + eps, highest scores kept within the budget;
+ *     item 5: Adaptive Neuron Balancer (lambda up on I/O stall, down on compute
+ *     stall); item 6: fused XOR/AND set update.
+ *
+ * Conventions for every call:
+ *   - Device pointers are plain CUDA device addresses on the CURRENT device;
+ *     host pointers are marked "host". Sizes are element counts unless named
+ *     *_bytes. The caller owns every per-call buffer; handles own the packed
+ *     weights and the momentum state.
+ *   - Index space is packed-slot order: slot s holds original neuron perm[s].
+ *     Neuron bitmask: slot i is bit (i % 32) of word (i / 32). Group bitmask:
+ *     group g is bit (g % 32) of word (g / 32). Group g = slots
+ *     [g*G, (g+1)*G). A group is active iff any of its slots is active.
+ *   - Hot calls (sffn_predict, sffn_forward, sffn_decode_step, tam_update,
+ *     tam_adapt) allocate nothing, never synchronize, only enqueue on the given
+ *     stream, and may be captured in a CUDA graph. They use programmatic
+ *     dependent launch between their own kernels.
+ *   - Errors are returned as sffn_status, never raised: argument checks are
+ *     synchronous and happen before any device work; a failed launch returns
+ *     SFFN_ERR_CUDA; conditions found on the device (a bounded wait that ran
+ *     out, an out-of-range index) set the handle's device error word, read by
+ *     sffn_layer_check_error / tam_check_error. sffn_last_error() gives a
+ *     thread-local description of the last failure.
+ */
+#ifndef SFFN_H_
+#define SFFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sffn_stream;   /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SFFN_OK = 0,
+  SFFN_ERR_INVALID_ARG = 1,   /* a pointer, size, alignment or enum is not allowed */
+  SFFN_ERR_UNSUPPORTED = 2,   /* valid, but not implemented by this build */
+  SFFN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  SFFN_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out */
+  SFFN_ERR_OOM = 5,           /* device allocation failed (create/pack only) */
+  SFFN_ERR_DEVICE = 6         /* the device found bad data (e.g. perm not a permutation) */
+} sffn_status;
+
+typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_REGLU = 1, SFFN_ACT_SWIGLU = 2 } sffn_act;
+typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
+
+/* Shape of one FFN layer and its predictor.
+ *   d: model dimension, multiple of 8, 8 <= d <= 16384.
+ *   f: FFN neurons, multiple of group_size, f / group_size <= 1024 groups.
+ *   h: predictor hidden size, multiple of 8, 8 <= h <= 4096.
+ *   group_size: 32 or 64 (KAIROX groups).
+ *   act: sffn_act. ReLU reads up and down; ReGLU and SwiGLU also read gate.
+ *   wdtype: storage type of every weight matrix (fp32 accumulation always).
+ *   max_batch: largest B the layer will be called with, 1..32. */
+typedef struct {
+  int32_t d, f, h, group_size;
+  int32_t act;
+  int32_t wdtype;
+  int32_t max_batch;
+} sffn_layer_desc;
+
+/* One token's (or a batch's) active-set views, all device buffers owned by the
+ * caller. Per-token arrays are laid out [B][...] with the stated row length:
+ *   nmask  [B][f/32]      neuron bitmask
+ *   gmask  [B][gw]        group bitmask, gw = ceil((f/G)/32)
+ *   idx    [B][f]         ascending active slots; entries past count[b] are untouched
+ *   count  [B]            number of active slots
+ * Batch union (only read or written when B > 1; may be NULL when B == 1):
+ *   unmask [f/32], ugmask [gw], uidx [f], ucount [1]. */
+typedef struct {
+  uint32_t* nmask;
+  uint32_t* gmask;
+  int32_t* idx;
+  int32_t* count;
+  uint32_t* unmask;
+  uint32_t* ugmask;
+  int32_t* uidx;
+  int32_t* ucount;
+} sffn_masks;
+
+typedef struct sffn_layer sffn_layer;
+typedef struct tam_state tam_state;
+
+/* Device addresses of a layer's packed arrays (read-only view, for tests and
+ * tools): W1 [h][d], b1 [h] (fp32, zeros if none), W2 [f][h] in slot order,
+ * b2 [f] (fp32, slot order, zeros if none), up/gate/downT [f][d] in slot order
+ * (gate NULL for ReLU; downT[s][:] is column perm[s] of down), perm [f]. */
+typedef struct {
+  const void* W1;
+  const float* b1;
+  const void* W2;
+  const float* b2;
+  const void* up;
+  const void* gate;
+  const void* downT;
+  const int32_t* perm;
+} sffn_packed_view;
+
+/* ---------------------------------------------------------------- status */
+
+const char* sffn_status_string(sffn_status s);
+/* Thread-local text of the last failure in this thread ("" if none). */
+const char* sffn_last_error(void);
+/* Library version string, e.g. "sffn 0.1 sm_103a". */
+const char* sffn_version(void);
+
+/* ---------------------------------------------------------------- layers */
+
+/* Host-only check of a layer description (no CUDA call). */
+sffn_status sffn_layer_validate(const sffn_layer_desc* desc);
+
+/* Create a layer on the current device: allocates the packed weight arrays
+ * (uninitialised until sffn_layer_pack) and a device error word. *out is set
+ * only on success. Errors: INVALID_ARG (desc), OOM, CUDA. */
+sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out);
+
+/* Pack row-major weights into the grouped, neuron-major layout (setup, not a
+ * hot call; synchronizes the stream before returning):
+ *   W1 [h][d], W2 [f][h] (row n = original neuron n), up [f][d],
+ *   gate [f][d] (NULL for ReLU, required otherwise), down [d][f] (column n =
+ *   original neuron n), all in the layer's wdtype; b1 [h], b2 [f] fp32 or NULL
+ *   (zero); perm [f] int32 with perm[slot] = original neuron id, or NULL for
+ *   the identity. Slot s of the packed arrays holds neuron perm[s]; down is
+ *   stored transposed so each neuron's output column is one contiguous row.
+ * Device pointers; 16-byte aligned. Errors: INVALID_ARG, DEVICE (perm is not
+ * a permutation of 0..f-1), OOM (temporary buffer), CUDA. */
+sffn_status sffn_layer_pack(sffn_layer* layer, const void* W1, const float* b1, const void* W2,
+                            const float* b2, const void* up, const void* gate, const void* down,
+                            const int32_t* perm, sffn_stream stream);
+
+sffn_status sffn_layer_get_desc(const sffn_layer* layer, sffn_layer_desc* out /* host */);
+sffn_status sffn_layer_packed(const sffn_layer* layer, sffn_packed_view* out /* host */);
+
+/* Bytes of device workspace that the hot calls need for batch size B
+ * (0 if the arguments are invalid). The workspace is caller-owned scratch,
+ * 256-byte aligned, reused across calls; its contents need no initialisation. */
+size_t sffn_workspace_bytes(const sffn_layer* layer, int32_t B);
+
+/* Synchronize the stream, then read and clear the layer's device error word:
+ * OK, TIMEOUT (a bounded wait ran out) or DEVICE (bad data seen on device). */
+sffn_status sffn_layer_check_error(const sffn_layer* layer, sffn_stream stream);
+
+void sffn_layer_destroy(sffn_layer* layer);
+
+/* Optional per-kernel timing hooks. Kernel slots: 0 predictor hidden layer,
+ * 1 predictor scores + threshold, 2 gather of up/gate rows + activation,
+ * 3 down projection. When set, every later hot call on this layer records
+ * begin[k] on its stream right before launching kernel k and end[k] right
+ * after it (NULL entries are skipped). The handles are cudaEvent_t values owned
+ * by the caller, which must keep them alive while tracing is on. Recording
+ * between two kernels removes their launch overlap, so traced timings bound
+ * each kernel alone. Pass NULL to turn tracing off. Host only; not
+ * thread-safe against hot calls on the same layer from other threads. */
+typedef struct {
+  void* begin[4];
+  void* end[4];
+} sffn_trace;
+
+sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* host, or NULL */);
+
+/* ---------------------------------------------------------------- hot calls */
+
+/* Predictor (PowerInfer §5.1 and the threshold note): for each token b,
+ *   hid = ReLU(W1 . x_b + b1), s = W2 . hid + b2, slot i active iff s_i >= thres
+ * (NaN is inactive), written as masks->nmask/gmask/idx/count for row b; for
+ * B > 1 also the union views. x: [B][d] fp32 device, 16-byte aligned.
+ * ws: workspace of at least sffn_workspace_bytes(layer, B).
+ * Errors: INVALID_ARG, UNSUPPORTED (B beyond what this build implements), CUDA. */
+sffn_status sffn_predict(const sffn_layer* layer, const float* x, int32_t B, float thres,
+                         const sffn_masks* masks, void* ws, size_t ws_bytes, sffn_stream stream);
+
+/* Sparse FFN over the active set given by masks->nmask (rows [B][f/32]; any
+ * caller-made mask is allowed): for each token b,
+ *   y_b = sum_{slot i active for b} act(gate_i . x_b, up_i . x_b) * downT_i
+ * with act = ReLU(u) | ReLU(g)*u | SiLU(g)*u, fp32 accumulation, fixed
+ * summation order (run-to-run bit-identical). Only active rows are read
+ * (PowerInfer §5.4). y: [B][d] fp32. x_out: NULL, or [B][d] fp32 that receives
+ * x + y (the residual stream of a layer stack). Other mask fields are ignored.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+sffn_status sffn_forward(const sffn_layer* layer, const float* x, int32_t B, const sffn_masks* masks,
+                         float* y, float* x_out, void* ws, size_t ws_bytes, sffn_stream stream);
+
+/* sffn_predict followed by sffn_forward on the predicted masks, as one
+ * pipelined sequence of kernels. All mask views are written. */
+sffn_status sffn_decode_step(const sffn_layer* layer, const float* x, int32_t B, float thres,
+                             const sffn_masks* masks, float* y, float* x_out, void* ws,
+                             size_t ws_bytes, sffn_stream stream);
+
+/* ---------------------------------------------------------------- TAM */
+
+/* Momentum state for n_layers layers of n_groups groups (1..1024): scores
+ * (fp32, start 0), lambda per layer (start lambda0, in (0, 1)), resident
+ * bitset (start empty), and a device error word. */
+sffn_status tam_create(int32_t n_layers, int32_t n_groups, float lambda0, tam_state** out);
+
+/* Outputs of tam_update; every pointer is optional (NULL = not written).
+ * Per-layer rows, n_layers rows each: bitsets [n][gw] with gw =
+ * ceil(n_groups/32); topk [n][capacity_k] group ids in rank order (score
+ * descending, then group id ascending), entries past n_res are -1;
+ * n_cand [n], n_res [n]. */
+typedef struct {
+  uint32_t* cand;
+  uint32_t* resident;
+  uint32_t* load;
+  uint32_t* evict;
+  uint32_t* changed;
+  int32_t* topk;
+  int32_t* n_cand;
+  int32_t* n_res;
+} tam_outputs;
+
+/* One momentum step for layers [layer0, layer0 + n_layers) (KAIROX 核心方法
+ * item 4), float32 with one rounding per operation and no fused multiply-add:
+ *   om = 1 - lambda; tau = om + eps;
+ *   s_g = lambda * s_g;  s_g = s_g + (group g active ? om : 0);
+ *   cand = {g : s_g > tau};  resident = the first capacity_k of cand ranked by
+ *   (s_g descending, g ascending);  load = res & ~prev;  evict = prev & ~res;
+ *   changed = res ^ prev;  the state's resident set becomes res.
+ * gmask: device, row l (for layer layer0 + l) starts at gmask + l*gmask_stride
+ * (words), gmask_stride >= gw. lambda < 0 uses each layer's state lambda.
+ * eps >= 0, capacity_k in [0, n_groups]. One thread block per layer.
+ * Errors: INVALID_ARG, CUDA. */
+sffn_status tam_update(tam_state* tam, int32_t layer0, int32_t n_layers, const uint32_t* gmask,
+                       int32_t gmask_stride, float lambda, float eps, int32_t capacity_k,
+                       const tam_outputs* out, sffn_stream stream);
+
+/* Adaptive Neuron Balancer step (KAIROX 核心方法 item 5) for layers
+ * [layer0, layer0 + n_layers): lambda_l <- min(hi, max(lo, lambda_l + (stall[l] ?
+ * +alpha : -alpha))) in float32, where stall [n_layers] uint8 device (nonzero =
+ * I/O stall). Requires 0 < lo <= hi < 1, alpha >= 0. */
+sffn_status tam_adapt(tam_state* tam, int32_t layer0, int32_t n_layers, const uint8_t* stall,
+                      float alpha, float lo, float hi, sffn_stream stream);
+
+/* Copy the state out of / into caller device buffers (checkpoint / resume):
+ * scores [n_layers][n_groups] fp32, lambdas [n_layers] fp32,
+ * resident [n_layers][gw] u32. Any pointer may be NULL (skipped). */
+sffn_status tam_get_state(const tam_state* tam, float* scores, float* lambdas, uint32_t* resident,
+                          sffn_stream stream);
+sffn_status tam_set_state(tam_state* tam, const float* scores, const float* lambdas,
+                          const uint32_t* resident, sffn_stream stream);
+sffn_status tam_get_shape(const tam_state* tam, int32_t* n_layers /* host */, int32_t* n_groups /* host */);
+sffn_status tam_check_error(const tam_state* tam, sffn_stream stream);
+void tam_destroy(tam_state* tam);
+
+/* ---------------------------------------------------------------- self-test */
+
+/* Exercise the bounded-wait path without any fault: one thread block waits
+ * on a shared-memory barrier that nothing will complete, gives up after
+ * limit_us microseconds (1..100000), records SFFN_ERR_TIMEOUT in the layer's
+ * device error word and returns. sffn_layer_check_error then reports TIMEOUT
+ * and the context stays usable. */
+sffn_status sffn_selftest_wait_timeout(const sffn_layer* layer, int32_t limit_us, sffn_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFFN_H_ */

@@ -198,6 +198,21 @@ def ffn_sparse(x: np.ndarray, up: np.ndarray, gate: np.ndarray | None, down: np.
     return y, h
 
 
+def ffn_sparse_stored(x: np.ndarray, up_s, gate_s, down_s, dtype: str, act: str, active: np.ndarray,
+                      perm=None) -> tuple[np.ndarray, np.ndarray]:
+    """:func:`ffn_sparse` on STORED weights (see :func:`widen`), widening only
+    the active rows of up/gate and columns of down, which keeps full-size
+    layers affordable. Same definition: the gathered rows are passed to
+    ffn_sparse with every gathered neuron active."""
+    f = up_s.shape[0]
+    perm = np.arange(f) if perm is None else np.asarray(perm)
+    orig = perm[np.flatnonzero(active)]
+    U = widen(up_s[orig], dtype)
+    G = widen(gate_s[orig], dtype) if gate_s is not None else None
+    D = widen(down_s[:, orig], dtype)
+    return ffn_sparse(x, U, G, D, act, np.ones(orig.shape[0], dtype=bool), None)
+
+
 # --------------------------------------------------------------------------
 # One layer, one or more tokens
 # --------------------------------------------------------------------------
