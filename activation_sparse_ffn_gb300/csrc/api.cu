@@ -136,7 +136,8 @@ sffn_status sffn_layer_validate(const sffn_layer_desc* desc) {
   if (D.act != SFFN_ACT_RELU && D.act != SFFN_ACT_REGLU && D.act != SFFN_ACT_SWIGLU) return invalid("act is not an sffn_act");
   if (D.d < 8 || D.d > 16384 || D.d % 8) return invalid("d must be a multiple of 8 in [8, 16384]");
   if ((long long)D.d * wbytes_of(D.wdtype) > 32768) return invalid("a weight row (d * element size) must be at most 32 KB");
-  if (D.h < 8 || D.h > 4096 || D.h % 8) return invalid("h must be a multiple of 8 in [8, 4096]");
+  if (D.h < 8 || D.h % 8) return invalid("h must be a positive multiple of 8");
+  if ((long long)D.h * wbytes_of(D.wdtype) > 2048) return invalid("a predictor row (h * element size) must be at most 2 KB");
   if (D.group_size != 32 && D.group_size != 64) return invalid("group_size must be 32 or 64");
   if (D.f < D.group_size || D.f % D.group_size) return invalid("f must be a positive multiple of group_size");
   if (D.f / D.group_size > 1024) return invalid("at most 1024 groups per layer");
@@ -163,6 +164,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   {
     const size_t stage = (size_t)desc->d * L->wbytes * (desc->act == SFFN_ACT_RELU ? 1 : 2);
     L->up_stages = (int)std::min<size_t>(8, std::max<size_t>(2, kUpSmemBudget / stage));
+    L->score_stages = score_stages_for(*L);
   }
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
@@ -196,6 +198,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   }
   e = cudaMemset(L->err, 0, 256);
   if (e == cudaSuccess) e = configure_kernels(*L);
+  if (e == cudaSuccess) e = configure_predict_kernels(*L);
   if (e != cudaSuccess) {
     rc = cuda_fail(e, "sffn_layer_create: kernel set-up");
     sffn_layer_destroy(L);

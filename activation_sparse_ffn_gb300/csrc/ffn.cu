@@ -161,7 +161,7 @@ template <typename T>
 __global__ void __launch_bounds__(kDownThreads, 1)
     k_down(const T* __restrict__ downT, const float* __restrict__ hval, const int32_t* __restrict__ alist,
            const int32_t* __restrict__ ws_count, const float* __restrict__ x, float* __restrict__ y,
-           float* __restrict__ x_out, int d, int W, int RS, int stages, uint32_t* __restrict__ err) {
+           float* __restrict__ x_out, int d, int W, int RS, int stages, int list_cap, uint32_t* __restrict__ err) {
   constexpr int NT = kDownThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   cg::cluster_group cluster = cg::this_cluster();
@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + down_region_bytes(W, sizeof(T), RS, stages, NT));
+  float* s_h = reinterpret_cast<float*>(full + stages);     // [list_cap] this block's h values
+  int32_t* s_slot = reinterpret_cast<int32_t*>(s_h + list_cap);  // [list_cap] and their slots
   __shared__ int s_issued;
 
   pdl_launch_dependents();
@@ -190,30 +192,37 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   const int total = *ws_count;
   const int lo = (int)((long long)total * rank / CL);
   const int hi = (int)((long long)total * (rank + 1) / CL);
-  const int n_local = hi - lo;
+  const int n_local = min(hi - lo, list_cap);
   const int nst = (n_local + RS - 1) / RS;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t pol = l2_policy_evict_first();
   const size_t col0 = (size_t)slice * W;
 
-  // warp 0 fills stage q: one row chunk per lane
-  auto issue = [&](int q) {
+  // warp 0 fills stage q: one row chunk per lane (slots from global memory
+  // for the first stages, from shared memory afterwards)
+  auto issue = [&](int q, bool from_global) {
     const int s = q % stages;
-    const int p0 = lo + q * RS;
-    const int nr = min(RS, hi - p0);
+    const int p0 = q * RS;
+    const int nr = min(RS, n_local - p0);
     if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nr * chunk_bytes);
     __syncwarp();
     if (lane < nr) {
-      const size_t slot = (size_t)alist[p0 + lane];
+      const size_t slot = (size_t)(from_global ? alist[lo + p0 + lane] : s_slot[p0 + lane]);
       bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)lane * chunk_bytes, downT + slot * d + col0, chunk_bytes,
                &full[s], pol);
     }
   };
   if (warp == 0) {
     const int first = min(stages, nst);
-    for (int q = 0; q < first; ++q) issue(q);
+    for (int q = 0; q < first; ++q) issue(q, true);
     if (lane == 0) s_issued = first;
   }
+  // this block's h values and slots, read once
+  for (int i = threadIdx.x; i < n_local; i += NT) {
+    s_h[i] = hval[lo + i];
+    s_slot[i] = alist[lo + i];
+  }
+  __syncthreads();
 
   float acc[EPC];
 #pragma unroll
@@ -223,12 +232,12 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   for (; q < nst; ++q) {
     const int s = q % stages;
     const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((q / stages) & 1));
-    const int p0 = lo + q * RS;
-    const int nr = min(RS, hi - p0);
+    const int p0 = q * RS;
+    const int nr = min(RS, n_local - p0);
     if (tr < RL) {
       const unsigned char* sp = ring + (size_t)s * stage_bytes + (size_t)tc * 16;
       for (int r = tr; r < nr; r += RL) {
-        const float hv = __ldg(hval + p0 + r);
+        const float hv = s_h[p0 + r];
         float w[EPC];
         WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)r * chunk_bytes), w);
 #pragma unroll
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
     if (warp == 0 && q + stages < nst) {
       if (lane == 0) fence_proxy_async_smem();
       __syncwarp();
-      issue(q + stages);
+      issue(q + stages, false);
       if (lane == 0) s_issued = q + stages + 1;
     }
   }
@@ -325,9 +334,11 @@ size_t gather_up_smem(const sffn_layer& L) {
          (size_t)up_list_cap(L) * 4;
 }
 
+int down_list_cap(const sffn_layer& L) { return (L.desc.f + kClusterSplit - 1) / kClusterSplit + 1; }
+
 size_t down_smem(const sffn_layer& L) {
   return down_region_bytes(L.down_width, L.wbytes, L.down_rows_per_stage, L.down_stages, kDownThreads) +
-         (size_t)L.down_stages * 8;
+         (size_t)L.down_stages * 8 + (size_t)down_list_cap(L) * 8;
 }
 
 cudaError_t configure_kernels(sffn_layer& L) {
@@ -385,7 +396,7 @@ cudaError_t launch_down(const sffn_layer& L, const float* hval, const int32_t* a
   const size_t smem = down_smem(L);
 #define SFFN_DOWN_ARGS                                                                                     \
   grid, dim3(kDownThreads), smem, st, true, kClusterSplit, static_cast<const T*>(L.downT), hval, alist,    \
-      ws_count, x, y, x_out, L.desc.d, L.down_width, L.down_rows_per_stage, L.down_stages, L.err
+      ws_count, x, y, x_out, L.desc.d, L.down_width, L.down_rows_per_stage, L.down_stages, down_list_cap(L), L.err
   switch (L.desc.wdtype) {
     case SFFN_F32: {
       using T = float;

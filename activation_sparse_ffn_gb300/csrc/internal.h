@@ -29,6 +29,7 @@ struct sffn_layer {
   uint32_t* err = nullptr;  // device error word
   bool has_b1 = false, has_b2 = false;
   // launch shapes chosen at create time
+  int score_stages = 0;     // predictor-scores ring depth (one mask word per stage)
   int up_stages = 0;        // gather-up ring depth
   int down_slices = 0;      // column slices of the down projection
   int down_width = 0;       // columns per slice
@@ -56,6 +57,7 @@ constexpr int kClusterSplit = 8;     // thread blocks per cluster in the down pr
 constexpr int kUpSmemBudget = 128 * 1024;
 constexpr int kDownStageBytes = 16 * 1024;
 constexpr int kDownSmemBudget = 80 * 1024;
+constexpr int kScoreSmemBudget = 192 * 1024;
 
 // Shared memory of the down projection: one region used first as the row
 // ring and then for the per-block column partials ([rows lanes][W] + [W]
@@ -105,6 +107,9 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
 
 // Shared memory sizes, set as kernel attributes at layer creation.
 cudaError_t configure_kernels(sffn_layer& L);
+cudaError_t configure_predict_kernels(const sffn_layer& L);
+int score_stages_for(const sffn_layer& L);
+size_t score_smem(const sffn_layer& L);
 size_t gather_up_smem(const sffn_layer& L);
 size_t down_smem(const sffn_layer& L);
 

@@ -7,20 +7,23 @@
 #include "internal.h"
 #include "scan.cuh"
 
+#include <algorithm>
+
 namespace sffn {
 
 namespace {
 
-constexpr int kHidRows = 8;      // predictor rows per thread block (stage 1)
+constexpr int kHidRows = 4;      // predictor rows per thread block (stage 1)
 constexpr int kHidThreads = 256;
-constexpr int kScoreThreads = 128;  // 4 warps per 32-row mask word (stage 2)
+constexpr int kScoreThreads = 128;  // 4 warps split the hidden dimension (stage 2)
 constexpr int kViewThreads = 1024;
 
 // Stage 1: each block computes kHidRows rows of hid. Thread t owns the
-// 16-byte chunks t, t+256, ... of every row, so the x values it needs are
-// the same for all rows; per-row partial sums are reduced across the block
-// in a fixed order.
-template <typename T>
+// 16-byte chunks t, t+256, ... of every row, so the x values it needs are the
+// same for all rows. The weights do not depend on the previous kernel, so all
+// of a thread's weight loads are issued into registers before waiting for x;
+// per-row partial sums are reduced across the block in a fixed order.
+template <typename T, int CPT>
 __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict__ W1, const float* __restrict__ b1,
                                                              const float* __restrict__ x, float* __restrict__ hid,
                                                              int h, int d) {
@@ -28,30 +31,35 @@ __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict
   const int r0 = blockIdx.x * kHidRows;
   const int nrows = min(kHidRows, h - r0);
   const T* base = W1 + (size_t)r0 * d;
-  // The weights do not depend on the previous kernel: start pulling this
-  // block's rows into L2 before waiting for x.
-  if (threadIdx.x == 0) prefetch_l2_bulk(base, (uint32_t)((size_t)nrows * d * sizeof(T)));
+  const int nch = d / EPC;
+  uint4 w[kHidRows][CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * kHidThreads;
+#pragma unroll
+    for (int r = 0; r < kHidRows; ++r)
+      if (r < nrows && c < nch) w[r][j] = ldg_stream(base + (size_t)r * d + (size_t)c * EPC);
+  }
   pdl_launch_dependents();
   pdl_wait();
 
-  const int nch = d / EPC;
   float acc[kHidRows];
 #pragma unroll
   for (int r = 0; r < kHidRows; ++r) acc[r] = 0.f;
-  for (int c = threadIdx.x; c < nch; c += kHidThreads) {
-    float xv[EPC];
 #pragma unroll
-    for (int e = 0; e < EPC; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(x + c * EPC + e);
-      xv[e] = v.x; xv[e + 1] = v.y; xv[e + 2] = v.z; xv[e + 3] = v.w;
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * kHidThreads;
+    if (c < nch) {
+      float xv[EPC];
+#pragma unroll
+      for (int e = 0; e < EPC; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(x + (size_t)c * EPC + e);
+        xv[e] = v.x; xv[e + 1] = v.y; xv[e + 2] = v.z; xv[e + 3] = v.w;
+      }
+#pragma unroll
+      for (int r = 0; r < kHidRows; ++r)
+        if (r < nrows) acc[r] += dot_chunk<T>(w[r][j], xv);
     }
-    uint4 w[kHidRows];
-#pragma unroll
-    for (int r = 0; r < kHidRows; ++r)
-      if (r < nrows) w[r] = ldg_stream(base + (size_t)r * d + (size_t)c * EPC);
-#pragma unroll
-    for (int r = 0; r < kHidRows; ++r)
-      if (r < nrows) acc[r] += dot_chunk<T>(w[r], xv);
   }
   __shared__ float red[kHidThreads / 32][kHidRows];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -64,7 +72,7 @@ __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict
   if (threadIdx.x < nrows) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kHidThreads / 32; ++w) s += red[w][threadIdx.x];
+    for (int w2 = 0; w2 < kHidThreads / 32; ++w2) s += red[w2][threadIdx.x];
     if (b1) s += b1[r0 + threadIdx.x];
     hid[r0 + threadIdx.x] = fmaxf(s, 0.f);
   }
@@ -85,56 +93,99 @@ __device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
   }
 }
 
-// Stage 2: one block per mask word (32 consecutive slots). Warp w covers the
-// w-th quarter of the hidden dimension for all 32 rows; lane sums are
-// reduce-scattered so lane i holds row i; the four warp partials are added in
-// a fixed order, the threshold is applied and one ballot gives the word.
+// Stage 2: persistent blocks, each owning a contiguous range of mask words
+// (32 consecutive slots = 32 contiguous W2 rows). The rows are streamed into a
+// shared-memory ring one word per stage by bulk copies; the first stages are
+// issued before waiting for hid. Warp w covers the w-th quarter of the hidden
+// dimension for all 32 rows; lane sums are reduce-scattered so lane i holds
+// row i; the four warp partials are added in a fixed order, the threshold is
+// applied and one ballot gives the word.
 template <typename T>
-__global__ void __launch_bounds__(kScoreThreads, 6) k_pred_scores(const T* __restrict__ W2,
+__global__ void __launch_bounds__(kScoreThreads, 1) k_pred_scores(const T* __restrict__ W2,
                                                                    const float* __restrict__ b2,
                                                                    const float* __restrict__ hid, float thres,
-                                                                   uint32_t* __restrict__ nmask, int h) {
+                                                                   uint32_t* __restrict__ nmask, int h, int nw,
+                                                                   int stages, uint32_t* __restrict__ err) {
   constexpr int EPC = WType<T>::kPerChunk;
-  const int word = blockIdx.x;
-  const T* base = W2 + (size_t)word * 32 * h;
-  if (threadIdx.x == 0) prefetch_l2_bulk(base, (uint32_t)((size_t)32 * h * sizeof(T)));
+  const int nb = gridDim.x, b = blockIdx.x;
+  const int w0 = (int)((long long)nw * b / nb), w1 = (int)((long long)nw * (b + 1) / nb);
+  const int nloc = w1 - w0;
+  const uint32_t row_bytes = (uint32_t)h * sizeof(T);
+  const uint32_t word_bytes = 32u * row_bytes;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* s_hid = reinterpret_cast<float*>(smem + (size_t)stages * word_bytes);  // 16-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_hid + h);
+  __shared__ float red[2][kScoreThreads / 32][32];
+  __shared__ int s_issued;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t pol = l2_policy_evict_first();
+  auto issue = [&](int k) {
+    const int s = k % stages;
+    mbar_arrive_expect_tx(&full[s], word_bytes);
+    bulk_g2s(smem + (size_t)s * word_bytes, W2 + (size_t)(w0 + k) * 32 * h, word_bytes, &full[s], pol);
+  };
+  if (threadIdx.x == 0) {
+    const int first = min(stages, nloc);
+    for (int k = 0; k < first; ++k) issue(k);
+    s_issued = first;
+  }
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait();  // hid comes from the previous kernel
+  for (int i = threadIdx.x * 4; i < h; i += kScoreThreads * 4)
+    *reinterpret_cast<float4*>(s_hid + i) = *reinterpret_cast<const float4*>(hid + i);
+  __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nch = h / EPC;
   const int cpw = (nch + 3) / 4;
   const int c0 = warp * cpw, c1 = min(nch, c0 + cpw);
-  float acc[32];
+  int k = 0;
+  bool aborted = false;
+  for (; k < nloc; ++k) {
+    const int s = k % stages;
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / stages) & 1));
+    const unsigned char* sp = smem + (size_t)s * word_bytes;
+    float acc[32];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) acc[r] = 0.f;
-  for (int c = c0 + lane; c < c1; c += 32) {
-    float hv[EPC];
+    for (int r = 0; r < 32; ++r) acc[r] = 0.f;
+    for (int c = c0 + lane; c < c1; c += 32) {
+      float hv[EPC];
 #pragma unroll
-    for (int e = 0; e < EPC; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(hid + c * EPC + e);
-      hv[e] = v.x; hv[e + 1] = v.y; hv[e + 2] = v.z; hv[e + 3] = v.w;
+      for (int e = 0; e < EPC; ++e) hv[e] = s_hid[c * EPC + e];
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        acc[r] += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)r * row_bytes + (size_t)c * 16), hv);
     }
+    transpose_reduce32(acc, lane);
+    red[k & 1][warp][lane] = acc[0];
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    if (warp == 0) {
+      float sc = red[k & 1][0][lane];
 #pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += 8) {
-      uint4 w[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) w[r] = ldg_stream(base + (size_t)(r0 + r) * h + (size_t)c * EPC);
-#pragma unroll
-      for (int r = 0; r < 8; ++r) acc[r0 + r] += dot_chunk<T>(w[r], hv);
+      for (int w2 = 1; w2 < kScoreThreads / 32; ++w2) sc += red[k & 1][w2][lane];
+      if (b2) sc += b2[(size_t)(w0 + k) * 32 + lane];
+      const uint32_t m = __ballot_sync(SFFN_FULL_MASK, sc >= thres);  // NaN compares false
+      if (lane == 0) {
+        nmask[w0 + k] = m;
+        if (k + stages < nloc) {
+          fence_proxy_async_smem();
+          issue(k + stages);
+          s_issued = k + stages + 1;
+        }
+      }
     }
   }
-  transpose_reduce32(acc, lane);
-  __shared__ float red[kScoreThreads / 32][32];
-  red[warp][lane] = acc[0];
-  __syncthreads();
-  if (warp == 0) {
-    float s = red[0][lane];
-#pragma unroll
-    for (int w = 1; w < kScoreThreads / 32; ++w) s += red[w][lane];
-    if (b2) s += b2[word * 32 + lane];
-    const uint32_t m = __ballot_sync(SFFN_FULL_MASK, s >= thres);  // NaN compares false
-    if (lane == 0) nmask[word] = m;
+  if (aborted && threadIdx.x == 0) {
+    set_device_error(err, SFFN_ERR_TIMEOUT);
+    for (int q = k; q < s_issued; ++q) mbar_wait_bounded(&full[q % stages], (uint32_t)((q / stages) & 1));
   }
 }
 
@@ -158,38 +209,70 @@ __global__ void __launch_bounds__(kViewThreads) k_mask_views(const uint32_t* __r
 
 }  // namespace
 
-cudaError_t launch_pred_hidden(const sffn_layer& L, const float* x, float* hid, cudaStream_t st) {
+namespace {
+
+int hid_cpt(const sffn_layer& L) {
+  const int nch = L.desc.d * L.wbytes / 16;
+  const int need = (nch + kHidThreads - 1) / kHidThreads;
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
+}
+
+template <typename T>
+cudaError_t launch_hidden_t(const sffn_layer& L, const float* x, float* hid, cudaStream_t st) {
   const int h = L.desc.h, d = L.desc.d;
-  dim3 grid((h + kHidRows - 1) / kHidRows);
+  const dim3 grid((h + kHidRows - 1) / kHidRows), block(kHidThreads);
+  const T* W1 = static_cast<const T*>(L.W1);
   const float* b1 = L.has_b1 ? L.b1 : nullptr;
+  switch (hid_cpt(L)) {
+    case 1: return launch_ex(k_pred_hidden<T, 1>, grid, block, 0, st, true, 1, W1, b1, x, hid, h, d);
+    case 2: return launch_ex(k_pred_hidden<T, 2>, grid, block, 0, st, true, 1, W1, b1, x, hid, h, d);
+    case 4: return launch_ex(k_pred_hidden<T, 4>, grid, block, 0, st, true, 1, W1, b1, x, hid, h, d);
+    default: return launch_ex(k_pred_hidden<T, 8>, grid, block, 0, st, true, 1, W1, b1, x, hid, h, d);
+  }
+}
+
+template <typename T>
+cudaError_t launch_scores_t(const sffn_layer& L, const float* hid, float thres, uint32_t* nmask, cudaStream_t st) {
+  const dim3 grid(std::min(L.nwords, L.num_sms)), block(kScoreThreads);
+  const float* b2 = L.has_b2 ? L.b2 : nullptr;
+  return launch_ex(k_pred_scores<T>, grid, block, score_smem(L), st, true, 1, static_cast<const T*>(L.W2), b2, hid,
+                   thres, nmask, L.desc.h, L.nwords, L.score_stages, L.err);
+}
+
+}  // namespace
+
+int score_stages_for(const sffn_layer& L) {
+  const size_t word = (size_t)32 * L.desc.h * L.wbytes;
+  return (int)std::min<size_t>(6, std::max<size_t>(2, kScoreSmemBudget / word));
+}
+
+size_t score_smem(const sffn_layer& L) {
+  return (size_t)L.score_stages * 32 * L.desc.h * L.wbytes + (size_t)L.score_stages * 8 + (size_t)L.desc.h * 4;
+}
+
+cudaError_t configure_predict_kernels(const sffn_layer& L) {
+  const int sm = (int)score_smem(L);
   switch (L.desc.wdtype) {
-    case SFFN_F32:
-      return launch_ex(k_pred_hidden<float>, grid, dim3(kHidThreads), 0, st, true, 1,
-                       static_cast<const float*>(L.W1), b1, x, hid, h, d);
-    case SFFN_F16:
-      return launch_ex(k_pred_hidden<__half>, grid, dim3(kHidThreads), 0, st, true, 1,
-                       static_cast<const __half*>(L.W1), b1, x, hid, h, d);
-    default:
-      return launch_ex(k_pred_hidden<__nv_bfloat16>, grid, dim3(kHidThreads), 0, st, true, 1,
-                       static_cast<const __nv_bfloat16*>(L.W1), b1, x, hid, h, d);
+    case SFFN_F32: return cudaFuncSetAttribute(k_pred_scores<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    case SFFN_F16: return cudaFuncSetAttribute(k_pred_scores<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    default: return cudaFuncSetAttribute(k_pred_scores<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  }
+}
+
+cudaError_t launch_pred_hidden(const sffn_layer& L, const float* x, float* hid, cudaStream_t st) {
+  switch (L.desc.wdtype) {
+    case SFFN_F32: return launch_hidden_t<float>(L, x, hid, st);
+    case SFFN_F16: return launch_hidden_t<__half>(L, x, hid, st);
+    default: return launch_hidden_t<__nv_bfloat16>(L, x, hid, st);
   }
 }
 
 cudaError_t launch_pred_scores(const sffn_layer& L, const float* hid, float thres, uint32_t* nmask,
                                cudaStream_t st) {
-  const int h = L.desc.h;
-  dim3 grid(L.nwords);
-  const float* b2 = L.has_b2 ? L.b2 : nullptr;
   switch (L.desc.wdtype) {
-    case SFFN_F32:
-      return launch_ex(k_pred_scores<float>, grid, dim3(kScoreThreads), 0, st, true, 1,
-                       static_cast<const float*>(L.W2), b2, hid, thres, nmask, h);
-    case SFFN_F16:
-      return launch_ex(k_pred_scores<__half>, grid, dim3(kScoreThreads), 0, st, true, 1,
-                       static_cast<const __half*>(L.W2), b2, hid, thres, nmask, h);
-    default:
-      return launch_ex(k_pred_scores<__nv_bfloat16>, grid, dim3(kScoreThreads), 0, st, true, 1,
-                       static_cast<const __nv_bfloat16*>(L.W2), b2, hid, thres, nmask, h);
+    case SFFN_F32: return launch_scores_t<float>(L, hid, thres, nmask, st);
+    case SFFN_F16: return launch_scores_t<__half>(L, hid, thres, nmask, st);
+    default: return launch_scores_t<__nv_bfloat16>(L, hid, thres, nmask, st);
   }
 }
 

@@ -398,7 +398,7 @@ class _DeviceArray:
     """Minimal __cuda_array_interface__ holder used to view a device address."""
 
     def __init__(self, ptr: int, shape: tuple, typestr: str):
-        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), True),
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), False),
                                          "version": 2, "strides": None}
 
 

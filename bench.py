@@ -45,6 +45,7 @@ def parse_args():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--layers", type=int, default=0, help="override the number of layers (0 = the workload's)")
     p.add_argument("--tokens", type=int, default=128, help="distinct tokens cycled through (one graph each)")
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--profile-steps", type=int, default=64)
@@ -170,6 +171,8 @@ def run_ours(args, world, rank, local):
     from activation_sparse_ffn_gb300 import workload as W
 
     spec = W.WORKLOADS[args.workload]
+    if args.layers:
+        spec = W.spec_replace(spec, layers=args.layers)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     nL = spec.layers

@@ -64,7 +64,8 @@ typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
 /* Shape of one FFN layer and its predictor.
  *   d: model dimension, multiple of 8, 8 <= d <= 16384.
  *   f: FFN neurons, multiple of group_size, f / group_size <= 1024 groups.
- *   h: predictor hidden size, multiple of 8, 8 <= h <= 4096.
+ *   h: predictor hidden size, multiple of 8, h * element size <= 2 KB
+ *      (h <= 1024 for 16-bit weights, h <= 512 for fp32).
  *   group_size: 32 or 64 (KAIROX groups).
  *   act: sffn_act. ReLU reads up and down; ReGLU and SwiGLU also read gate.
  *   wdtype: storage type of every weight matrix (fp32 accumulation always).

@@ -60,6 +60,8 @@ def test_status_strings(lib):
     (dict(d=512, f=2048, h=64, group_size=48, act="relu", wdtype="f32"), False),     # G
     (dict(d=512, f=65600, h=64, group_size=32, act="relu", wdtype="f16"), False),    # > 1024 groups
     (dict(d=512, f=2048, h=12, group_size=32, act="relu", wdtype="f32"), False),     # h % 8
+    (dict(d=512, f=2048, h=1024, group_size=32, act="relu", wdtype="f32"), False),   # predictor row > 2 KB
+    (dict(d=512, f=2048, h=1024, group_size=32, act="relu", wdtype="bf16"), True),
     (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="f32", max_batch=33), False),
     (dict(d=512, f=2048, h=64, group_size=32, act=7, wdtype="f32"), False),
     (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype=9), False),
