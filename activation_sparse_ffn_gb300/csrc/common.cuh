@@ -48,6 +48,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -112,7 +116,20 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// 16-byte streaming load that does not allocate in L1.
+// Loads of data written by an earlier kernel of the same stream, in
+// particular by the programmatic-launch predecessor that this kernel waits for
+// with griddepcontrol.wait. Such data is not read-only for this kernel's
+// lifetime (the kernel starts before its predecessor finishes), so it must
+// never go through the non-coherent read-only path (ld.global.nc, which
+// `const __restrict__` pointers invite) or a possibly stale L1 line: these
+// loads read from L2, the point of coherence, and are issued only after the
+// wait.
+__device__ __forceinline__ float ld_dep(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ int ld_dep(const int* p) { return __ldcg(p); }
+__device__ __forceinline__ uint32_t ld_dep(const uint32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ float4 ld_dep4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// 16-byte streaming load that does not allocate in L1 (immutable weights only).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -183,11 +200,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ReLU that propagates NaN (fmaxf would turn NaN into 0).
+__device__ __forceinline__ float relu_nan(float v) { return v < 0.f ? 0.f : v; }
+
 // Activation of one neuron from its up value u and gate value g.
 template <int ACT>
 __device__ __forceinline__ float neuron_act(float u, float g) {
-  if (ACT == SFFN_ACT_RELU) return fmaxf(u, 0.f);
-  if (ACT == SFFN_ACT_REGLU) return fmaxf(g, 0.f) * u;
+  if (ACT == SFFN_ACT_RELU) return relu_nan(u);
+  if (ACT == SFFN_ACT_REGLU) return relu_nan(g) * u;
   return g / (1.f + expf(-g)) * u;  // SiLU(g) * u
 }
 

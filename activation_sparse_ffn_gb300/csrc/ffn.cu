@@ -23,13 +23,23 @@ namespace sffn {
 
 namespace {
 
-constexpr int kUpThreads = 256;
-constexpr int kDownThreads = 256;
+constexpr int kConsumerWarps = 8;
+constexpr int kUpThreads = (kConsumerWarps + 1) * 32;    // 8 consumer warps + 1 producer warp
+constexpr int kDownThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
 
+// Gather of the active up/gate rows. Warp 8 is the producer: one lane issues
+// the bulk copies of neuron k's rows into ring stage k % S once the consumer
+// warps have released that stage (empty barrier, one arrival per warp). The
+// eight consumer warps wait for each stage (full barrier, transaction bytes),
+// form their partial dot products with the x chunks they own, store one
+// partial per warp in shared memory and release the stage; no block-wide
+// barrier inside the loop. After the loop the partials of every neuron are
+// summed in a fixed order and the activation is applied.
 template <typename T, int ACT, int CPT>
 __global__ void __launch_bounds__(kUpThreads, 1)
-    k_gather_up(const T* __restrict__ up, const T* __restrict__ gate, const float* __restrict__ x,
-                const uint32_t* __restrict__ nmask, int nw, int n_groups, int G, int gwords, int d, int stages,
+    k_gather_up(const T* __restrict__ up, const T* __restrict__ gate, const float* x,
+                const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages,
                 int list_cap, int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out,
                 uint32_t* __restrict__ gmask_out, float* __restrict__ hval, int32_t* __restrict__ alist,
                 int32_t* __restrict__ ws_count, uint32_t* __restrict__ err) {
@@ -43,17 +53,22 @@ __global__ void __launch_bounds__(kUpThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * stage_bytes);
-  uint32_t* s_words = reinterpret_cast<uint32_t*>(full + stages);
+  uint64_t* empty = full + stages;
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(empty + stages);
   int* s_off = reinterpret_cast<int*>(s_words + nw);
   int32_t* s_list = reinterpret_cast<int32_t*>(s_off + nw);
+  float* s_part = reinterpret_cast<float*>(s_list + list_cap);  // [list_cap][warps][2]
   __shared__ int s_tmp[NT / 32];
-  __shared__ float s_red[2][NT / 32][2];
-  __shared__ int s_issued;
+  __shared__ int s_abort;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
     fence_mbar_init();
+    s_abort = 0;
   }
   pdl_wait();  // the mask comes from the previous kernel
 
@@ -72,97 +87,102 @@ __global__ void __launch_bounds__(kUpThreads, 1)
   }
   __syncthreads();
 
-  const uint64_t pol = l2_policy_evict_first();
-  auto issue = [&](int k) {
-    const int s = k % stages;
-    const size_t slot = (size_t)s_list[k];
-    unsigned char* dst = ring + (size_t)s * stage_bytes;
-    mbar_arrive_expect_tx(&full[s], stage_bytes);
-    bulk_g2s(dst, up + slot * d, row_bytes, &full[s], pol);
-    if (GATED) bulk_g2s(dst + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
-  };
-  if (threadIdx.x == 0) {
-    const int first = min(stages, n_local);
-    for (int k = 0; k < first; ++k) issue(k);
-    s_issued = first;
-  }
-  for (int k = threadIdx.x; k < n_local; k += NT) {
-    const int s = s_list[k];
-    alist[lo + k] = s;
-    if (idx_out) idx_out[lo + k] = s;
-  }
-
-  // this thread's chunks of x, fixed for every row
-  float xr[CPT][EPC];
-#pragma unroll
-  for (int j = 0; j < CPT; ++j) {
-    const int c = threadIdx.x + j * NT;
-#pragma unroll
-    for (int e = 0; e < EPC; e += 4) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c < nch) v = *reinterpret_cast<const float4*>(x + (size_t)c * EPC + e);
-      xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
-    }
-  }
-
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int k = 0;
-  bool aborted = false;
-  for (; k < n_local; ++k) {
-    const int s = k % stages;
-    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / stages) & 1));
-    const unsigned char* sp = ring + (size_t)s * stage_bytes;
-    float pu = 0.f, pg = 0.f;
+  if (warp == kConsumerWarps) {
+    // ---------------- producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int k = 0; k < n_local; ++k) {
+        const int s = k % stages;
+        const bool ok = k < stages || mbar_wait_bounded(&empty[s], (uint32_t)((k / stages - 1) & 1));
+        if (!ok || *(volatile int*)&s_abort) {
+          if (!ok) set_device_error(err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+          // drain: let the copies that may still be in flight land
+          for (int q = max(0, k - stages); q < k; ++q) mbar_wait_bounded(&full[q % stages], (uint32_t)((q / stages) & 1));
+          break;
+        }
+        const size_t slot = (size_t)s_list[k];
+        unsigned char* dst = ring + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        bulk_g2s(dst, up + slot * d, row_bytes, &full[s], pol);
+        if (GATED) bulk_g2s(dst + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+      }
+    }
+  } else {
+    // ---------------- consumers: this thread's chunks of x, fixed for every row
+    float xr[CPT][EPC];
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
-      const int c = threadIdx.x + j * NT;
-      if (c < nch) {
-        const uint4 wu = *reinterpret_cast<const uint4*>(sp + (size_t)c * 16);
-        pu += dot_chunk<T>(wu, xr[j]);
-        if (GATED) {
-          const uint4 wg = *reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16);
-          pg += dot_chunk<T>(wg, xr[j]);
+      const int c = threadIdx.x + j * kConsumers;
+#pragma unroll
+      for (int e = 0; e < EPC; e += 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < nch) v = ld_dep4(x + (size_t)c * EPC + e);
+        xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
+      }
+    }
+    for (int k = 0; k < n_local; ++k) {
+      const int s = k % stages;
+      // warp-uniform outcome: the shuffles below need every lane
+      const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((k / stages) & 1)));
+      if (!ok) {
+        if (lane == 0) {
+          set_device_error(err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      if (__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) break;
+      const unsigned char* sp = ring + (size_t)s * stage_bytes;
+      float pu = 0.f, pg = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const int c = threadIdx.x + j * kConsumers;
+        if (c < nch) {
+          pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
+          if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
         }
       }
-    }
-    pu = warp_sum(pu);
-    if (GATED) pg = warp_sum(pg);
-    if (lane == 0) {
-      s_red[k & 1][warp][0] = pu;
-      s_red[k & 1][warp][1] = pg;
-    }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    if (threadIdx.x == 0) {
-      float u = 0.f, g = 0.f;
-#pragma unroll
-      for (int w = 0; w < NT / 32; ++w) {
-        u += s_red[k & 1][w][0];
-        g += s_red[k & 1][w][1];
+      pu = warp_sum(pu);
+      if (GATED) pg = warp_sum(pg);
+      if (lane == 0) {
+        s_part[((size_t)k * kConsumerWarps + warp) * 2] = pu;
+        s_part[((size_t)k * kConsumerWarps + warp) * 2 + 1] = pg;
       }
-      hval[lo + k] = neuron_act<ACT>(u, g);
-      if (k + stages < n_local) {
-        fence_proxy_async_smem();
-        issue(k + stages);
-        s_issued = k + stages + 1;
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
-  if (aborted && threadIdx.x == 0) {
-    set_device_error(err, SFFN_ERR_TIMEOUT);
-    // let the copies already in flight land before the block exits
-    for (int q = k; q < s_issued; ++q) mbar_wait_bounded(&full[q % stages], (uint32_t)((q / stages) & 1));
+  __syncthreads();
+  if (s_abort) return;
+  for (int k = threadIdx.x; k < n_local; k += NT) {
+    float u = 0.f, g = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      u += s_part[((size_t)k * kConsumerWarps + w) * 2];
+      g += s_part[((size_t)k * kConsumerWarps + w) * 2 + 1];
+    }
+    hval[lo + k] = neuron_act<ACT>(u, g);
+    const int sl = s_list[k];
+    alist[lo + k] = sl;
+    if (idx_out) idx_out[lo + k] = sl;
   }
 }
 
+// Down projection, y = sum_i h_i * downT_i. Thread-block clusters of eight
+// split the active list; the grid's second dimension splits d into column
+// slices. The producer warp streams each row's slice chunk into the ring
+// (one lane per row); the consumer warps accumulate h_i * chunk in registers
+// (each thread owns one 16-byte column chunk and a set of rows) and release
+// stages through the empty barriers. Afterwards the row lanes are summed in
+// shared memory and the eight blocks' partials are added through distributed
+// shared memory in rank order.
 template <typename T>
 __global__ void __launch_bounds__(kDownThreads, 1)
-    k_down(const T* __restrict__ downT, const float* __restrict__ hval, const int32_t* __restrict__ alist,
-           const int32_t* __restrict__ ws_count, const float* __restrict__ x, float* __restrict__ y,
+    k_down(const T* __restrict__ downT, const float* hval, const int32_t* alist,
+           const int32_t* ws_count, const float* x, float* __restrict__ y,
            float* __restrict__ x_out, int d, int W, int RS, int stages, int list_cap, uint32_t* __restrict__ err) {
-  constexpr int NT = kDownThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = (int)cluster.num_blocks();
@@ -170,122 +190,123 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   const int slice = blockIdx.y;
   const uint32_t chunk_bytes = (uint32_t)W * sizeof(T);
   const int CPR = (int)(chunk_bytes / 16);
-  const int RL = NT / CPR;
+  const int RL = kConsumers / CPR;
   const int tc = threadIdx.x % CPR, tr = threadIdx.x / CPR;
   const uint32_t stage_bytes = (uint32_t)RS * chunk_bytes;
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + down_region_bytes(W, sizeof(T), RS, stages, NT));
-  float* s_h = reinterpret_cast<float*>(full + stages);     // [list_cap] this block's h values
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + down_region_bytes(W, sizeof(T), RS, stages, kConsumers));
+  uint64_t* empty = full + stages;
+  float* s_h = reinterpret_cast<float*>(empty + stages);     // [list_cap] this block's h values
   int32_t* s_slot = reinterpret_cast<int32_t*>(s_h + list_cap);  // [list_cap] and their slots
-  __shared__ int s_issued;
+  __shared__ int s_abort;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
     fence_mbar_init();
+    s_abort = 0;
   }
   __syncthreads();
   pdl_wait();  // h values and the active list come from the previous kernel
 
-  const int total = *ws_count;
+  const int total = ld_dep(ws_count);
   const int lo = (int)((long long)total * rank / CL);
   const int hi = (int)((long long)total * (rank + 1) / CL);
   const int n_local = min(hi - lo, list_cap);
   const int nst = (n_local + RS - 1) / RS;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint64_t pol = l2_policy_evict_first();
   const size_t col0 = (size_t)slice * W;
-
-  // warp 0 fills stage q: one row chunk per lane (slots from global memory
-  // for the first stages, from shared memory afterwards)
-  auto issue = [&](int q, bool from_global) {
-    const int s = q % stages;
-    const int p0 = q * RS;
-    const int nr = min(RS, n_local - p0);
-    if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nr * chunk_bytes);
-    __syncwarp();
-    if (lane < nr) {
-      const size_t slot = (size_t)(from_global ? alist[lo + p0 + lane] : s_slot[p0 + lane]);
-      bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)lane * chunk_bytes, downT + slot * d + col0, chunk_bytes,
-               &full[s], pol);
-    }
-  };
-  if (warp == 0) {
-    const int first = min(stages, nst);
-    for (int q = 0; q < first; ++q) issue(q, true);
-    if (lane == 0) s_issued = first;
-  }
-  // this block's h values and slots, read once
-  for (int i = threadIdx.x; i < n_local; i += NT) {
-    s_h[i] = hval[lo + i];
-    s_slot[i] = alist[lo + i];
+  for (int i = threadIdx.x; i < n_local; i += kDownThreads) {
+    s_h[i] = ld_dep(hval + lo + i);
+    s_slot[i] = ld_dep(alist + lo + i);
   }
   __syncthreads();
 
   float acc[EPC];
 #pragma unroll
   for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
-  int q = 0;
-  bool aborted = false;
-  for (; q < nst; ++q) {
-    const int s = q % stages;
-    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((q / stages) & 1));
-    const int p0 = q * RS;
-    const int nr = min(RS, n_local - p0);
-    if (tr < RL) {
-      const unsigned char* sp = ring + (size_t)s * stage_bytes + (size_t)tc * 16;
-      for (int r = tr; r < nr; r += RL) {
-        const float hv = s_h[p0 + r];
-        float w[EPC];
-        WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)r * chunk_bytes), w);
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[e] = fmaf(hv, w[e], acc[e]);
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: stage q = rows [q*RS, q*RS + RS), one lane per row
+    const uint64_t pol = l2_policy_evict_first();
+    for (int q = 0; q < nst; ++q) {
+      const int s = q % stages;
+      const bool ok = __all_sync(SFFN_FULL_MASK, q < stages || mbar_wait_bounded(&empty[s], (uint32_t)((q / stages - 1) & 1)));
+      if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+        if (lane == 0) {
+          if (!ok) set_device_error(err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+          // drain: let the copies that may still be in flight land
+          for (int r = max(0, q - stages); r < q; ++r) mbar_wait_bounded(&full[r % stages], (uint32_t)((r / stages) & 1));
+        }
+        break;
       }
-    }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    if (warp == 0 && q + stages < nst) {
-      if (lane == 0) fence_proxy_async_smem();
+      const int p0 = q * RS;
+      const int nr = min(RS, n_local - p0);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nr * chunk_bytes);
       __syncwarp();
-      issue(q + stages, false);
-      if (lane == 0) s_issued = q + stages + 1;
+      if (lane < nr)
+        bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)lane * chunk_bytes, downT + (size_t)s_slot[p0 + lane] * d + col0,
+                 chunk_bytes, &full[s], pol);
+    }
+  } else {
+    // ---------------- consumers
+    for (int q = 0; q < nst; ++q) {
+      const int s = q % stages;
+      const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((q / stages) & 1)));
+      if (!ok) {
+        if (lane == 0) {
+          set_device_error(err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      if (__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) break;
+      const int p0 = q * RS;
+      const int nr = min(RS, n_local - p0);
+      if (tr < RL) {
+        const unsigned char* sp = ring + (size_t)s * stage_bytes + (size_t)tc * 16;
+        for (int r = tr; r < nr; r += RL) {
+          const float hv = s_h[p0 + r];
+          float w[EPC];
+          WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)r * chunk_bytes), w);
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) acc[e] = fmaf(hv, w[e], acc[e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
-  if (aborted) {
-    if (threadIdx.x == 0) {
-      set_device_error(err, SFFN_ERR_TIMEOUT);
-      for (int r = q; r < s_issued; ++r) mbar_wait_bounded(&full[r % stages], (uint32_t)((r / stages) & 1));
-    }
-    __syncthreads();
-  }
+  __syncthreads();
 
   // per-block partial of this column slice: reduce the row lanes in order
   // (the ring region is free once every stage has been consumed)
   float* red = reinterpret_cast<float*>(ring);          // [RL][W]
   float* part = red + (size_t)RL * W;                   // [W]
-  if (tr < RL) {
+  if (warp < kConsumerWarps && tr < RL) {
 #pragma unroll
     for (int e = 0; e < EPC; ++e) red[(size_t)tr * W + tc * EPC + e] = acc[e];
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < W; j += NT) {
-    float s = 0.f;
-    for (int r = 0; r < RL; ++r) s += red[(size_t)r * W + j];
-    part[j] = s;
+  for (int j = threadIdx.x; j < W; j += kDownThreads) {
+    float sum = 0.f;
+    for (int r = 0; r < RL; ++r) sum += red[(size_t)r * W + j];
+    part[j] = sum;
   }
   cluster.sync();
   // rank r finishes columns [j0, j1) of the slice, adding the partials of
   // ranks 0..CL-1 in order
   const int j0 = (int)((long long)W * rank / CL), j1 = (int)((long long)W * (rank + 1) / CL);
-  for (int j = j0 + threadIdx.x; j < j1; j += NT) {
-    float s = 0.f;
-    for (int r = 0; r < CL; ++r) s += cluster.map_shared_rank(part, r)[j];
-    y[col0 + j] = s;
-    if (x_out) x_out[col0 + j] = x[col0 + j] + s;
+  for (int j = j0 + threadIdx.x; j < j1; j += kDownThreads) {
+    float sum = 0.f;
+    for (int r = 0; r < CL; ++r) sum += cluster.map_shared_rank(part, r)[j];
+    y[col0 + j] = sum;
+    if (x_out) x_out[col0 + j] = ld_dep(x + col0 + j) + sum;
   }
   cluster.sync();
 }
@@ -319,7 +340,7 @@ cudaError_t set_up_attr(size_t smem) {
 
 int up_cpt(const sffn_layer& L) {
   const int nch = L.desc.d * L.wbytes / 16;
-  const int need = (nch + kUpThreads - 1) / kUpThreads;
+  const int need = (nch + kConsumers - 1) / kConsumers;
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
 }
 
@@ -330,15 +351,15 @@ int up_list_cap(const sffn_layer& L) { return (L.desc.f + L.num_sms - 1) / L.num
 size_t gather_up_smem(const sffn_layer& L) {
   const size_t row = (size_t)L.desc.d * L.wbytes;
   const size_t stage = row * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
-  return (size_t)L.up_stages * stage + (size_t)L.up_stages * 8 + (size_t)L.nwords * 8 +
-         (size_t)up_list_cap(L) * 4;
+  return (size_t)L.up_stages * stage + (size_t)L.up_stages * 16 + (size_t)L.nwords * 8 +
+         (size_t)up_list_cap(L) * 4 + (size_t)up_list_cap(L) * kConsumerWarps * 2 * 4;
 }
 
 int down_list_cap(const sffn_layer& L) { return (L.desc.f + kClusterSplit - 1) / kClusterSplit + 1; }
 
 size_t down_smem(const sffn_layer& L) {
-  return down_region_bytes(L.down_width, L.wbytes, L.down_rows_per_stage, L.down_stages, kDownThreads) +
-         (size_t)L.down_stages * 8 + (size_t)down_list_cap(L) * 8;
+  return down_region_bytes(L.down_width, L.wbytes, L.down_rows_per_stage, L.down_stages, kConsumers) +
+         (size_t)L.down_stages * 16 + (size_t)down_list_cap(L) * 8;
 }
 
 cudaError_t configure_kernels(sffn_layer& L) {

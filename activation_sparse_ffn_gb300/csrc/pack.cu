@@ -123,6 +123,7 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
     if (herr) {
       set_error("sffn_layer_pack: perm is not a permutation of 0..f-1");
       rc = SFFN_ERR_DEVICE;
+      cudaMemsetAsync(L.err, 0, sizeof(uint32_t), st);  // reported here, so cleared
       goto done;
     }
     SFFN_TRY(cudaMemcpyAsync(L.perm, perm, (size_t)f * 4, cudaMemcpyDeviceToDevice, st), "pack: perm");
@@ -156,6 +157,7 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
   if (herr) {
     set_error("sffn_layer_pack: a device check failed while packing");
     rc = (sffn_status)herr;
+    cudaMemsetAsync(L.err, 0, sizeof(uint32_t), st);  // reported here, so cleared
   }
 #undef SFFN_TRY
 done:

@@ -25,7 +25,7 @@ constexpr int kViewThreads = 1024;
 // per-row partial sums are reduced across the block in a fixed order.
 template <typename T, int CPT>
 __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict__ W1, const float* __restrict__ b1,
-                                                             const float* __restrict__ x, float* __restrict__ hid,
+                                                             const float* x, float* __restrict__ hid,
                                                              int h, int d) {
   constexpr int EPC = WType<T>::kPerChunk;
   const int r0 = blockIdx.x * kHidRows;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict
       float xv[EPC];
 #pragma unroll
       for (int e = 0; e < EPC; e += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(x + (size_t)c * EPC + e);
+        const float4 v = ld_dep4(x + (size_t)c * EPC + e);
         xv[e] = v.x; xv[e + 1] = v.y; xv[e + 2] = v.z; xv[e + 3] = v.w;
       }
 #pragma unroll
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kHidThreads) k_pred_hidden(const T* __restrict
 #pragma unroll
     for (int w2 = 0; w2 < kHidThreads / 32; ++w2) s += red[w2][threadIdx.x];
     if (b1) s += b1[r0 + threadIdx.x];
-    hid[r0 + threadIdx.x] = fmaxf(s, 0.f);
+    hid[r0 + threadIdx.x] = relu_nan(s);
   }
 }
 
@@ -103,7 +103,7 @@ __device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
 template <typename T>
 __global__ void __launch_bounds__(kScoreThreads, 1) k_pred_scores(const T* __restrict__ W2,
                                                                    const float* __restrict__ b2,
-                                                                   const float* __restrict__ hid, float thres,
+                                                                   const float* hid, float thres,
                                                                    uint32_t* __restrict__ nmask, int h, int nw,
                                                                    int stages, uint32_t* __restrict__ err) {
   constexpr int EPC = WType<T>::kPerChunk;
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_pred_scores(const T* __res
   pdl_launch_dependents();
   pdl_wait();  // hid comes from the previous kernel
   for (int i = threadIdx.x * 4; i < h; i += kScoreThreads * 4)
-    *reinterpret_cast<float4*>(s_hid + i) = *reinterpret_cast<const float4*>(hid + i);
+    *reinterpret_cast<float4*>(s_hid + i) = ld_dep4(hid + i);
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) k_pred_scores(const T* __res
 
 // Expands a neuron bitmask into the ascending index list, the count and the
 // group bitmask (single block).
-__global__ void __launch_bounds__(kViewThreads) k_mask_views(const uint32_t* __restrict__ nmask, int nw,
+__global__ void __launch_bounds__(kViewThreads) k_mask_views(const uint32_t* nmask, int nw,
                                                              int n_groups, int G, int gwords,
                                                              int32_t* __restrict__ idx, int32_t* __restrict__ count,
                                                              uint32_t* __restrict__ gmask) {

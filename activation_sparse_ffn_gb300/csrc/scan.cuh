@@ -40,13 +40,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_tmp, int* tota
 // Loads nw mask words into s_words and writes each word's offset in the
 // ascending active list into s_off. Returns the number of active slots.
 template <int NT>
-__device__ __forceinline__ int scan_mask_words(const uint32_t* __restrict__ nmask, int nw, uint32_t* s_words,
+__device__ __forceinline__ int scan_mask_words(const uint32_t* nmask, int nw, uint32_t* s_words,
                                                int* s_off, int* s_tmp) {
   const int per = (nw + NT - 1) / NT;
   const int w0 = min(nw, (int)threadIdx.x * per), w1 = min(nw, w0 + per);
   int local = 0;
   for (int w = w0; w < w1; ++w) {
-    const uint32_t m = nmask[w];
+    const uint32_t m = ld_dep(nmask + w);  // written by the previous kernel
     s_words[w] = m;
     local += __popc(m);
   }

@@ -19,8 +19,8 @@ namespace {
 constexpr int kTamThreads = 1024;
 
 __global__ void __launch_bounds__(kTamThreads)
-    k_tam_update(float* __restrict__ scores, const float* __restrict__ lambdas, uint32_t* __restrict__ resident,
-                 int n_groups, int gwords, const uint32_t* __restrict__ gmask, int gstride, int layer0,
+    k_tam_update(float* scores, const float* lambdas, uint32_t* resident,
+                 int n_groups, int gwords, const uint32_t* gmask, int gstride, int layer0,
                  float lambda_arg, float eps, int K, tam_outputs out) {
   pdl_launch_dependents();
   pdl_wait();
@@ -31,15 +31,15 @@ __global__ void __launch_bounds__(kTamThreads)
   __shared__ unsigned long long keys[kTamThreads];
   __shared__ uint32_t s_cand[32], s_res[32];
 
-  const float lam = lambda_arg >= 0.f ? lambda_arg : lambdas[layer];
+  const float lam = lambda_arg >= 0.f ? lambda_arg : ld_dep(lambdas + layer);
   const float om = __fsub_rn(1.0f, lam);
   const float tau = __fadd_rn(om, eps);
   float s = 0.f;
   bool c = false;
   if (g < n_groups) {
     float* sp = scores + (size_t)layer * n_groups + g;
-    const bool active = (gmask[(size_t)l * gstride + (g >> 5)] >> (g & 31)) & 1u;
-    s = __fmul_rn(lam, *sp);
+    const bool active = (ld_dep(gmask + (size_t)l * gstride + (g >> 5)) >> (g & 31)) & 1u;
+    s = __fmul_rn(lam, ld_dep(sp));
     s = __fadd_rn(s, active ? om : 0.0f);
     *sp = s;
     c = s > tau;
@@ -47,24 +47,42 @@ __global__ void __launch_bounds__(kTamThreads)
   const uint32_t cw = __ballot_sync(SFFN_FULL_MASK, c);
   if (lane == 0) s_cand[warp] = cw;
   if (g < 32) s_res[g] = 0u;
-  keys[g] = c ? ((unsigned long long)__float_as_uint(s) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)g)
-              : 0ull;
+  unsigned long long key =
+      c ? ((unsigned long long)__float_as_uint(s) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)g) : 0ull;
   const int nc = __syncthreads_count(c);
-  // bitonic sort, descending
+  // Bitonic sort, descending. Partner distances j >= 32 exchange through
+  // shared memory (one barrier per step); j < 32 exchange with warp shuffles.
+  // In a block of size k that sorts descending ((g & k) == 0) the lower index
+  // of each pair keeps the larger key; in an ascending block, the smaller.
   for (int k = 2; k <= kTamThreads; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const int p = g ^ j;
-      if (p > g) {
-        const unsigned long long a = keys[g], b = keys[p];
-        const bool desc = (g & k) == 0;
-        if (desc ? (a < b) : (a > b)) {
-          keys[g] = b;
-          keys[p] = a;
+    const bool desc = (g & k) == 0;
+    int j = k >> 1;
+    if (j >= 32) {
+      keys[g] = key;
+      __syncthreads();
+      for (; j >= 32; j >>= 1) {
+        const int p = g ^ j;
+        if (p > g) {
+          const unsigned long long a = keys[g], b = keys[p];
+          if (desc ? (a < b) : (a > b)) {
+            keys[g] = b;
+            keys[p] = a;
+          }
         }
+        __syncthreads();
       }
+      key = keys[g];
       __syncthreads();
     }
+    for (; j > 0; j >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(SFFN_FULL_MASK, key, j);
+      const bool lower = (g & j) == 0;
+      const unsigned long long hi = key > other ? key : other, lo2 = key > other ? other : key;
+      key = (lower == desc) ? hi : lo2;
+    }
   }
+  keys[g] = key;
+  __syncthreads();
   const int nres = min(K, nc);
   int gid = -1;
   if (g < nres) {
@@ -75,7 +93,7 @@ __global__ void __launch_bounds__(kTamThreads)
   __syncthreads();
   if (g < gwords) {
     uint32_t* rp = resident + (size_t)layer * gwords + g;
-    const uint32_t prev = *rp, res = s_res[g];
+    const uint32_t prev = ld_dep(rp), res = s_res[g];
     const size_t o = (size_t)l * gwords + g;
     if (out.cand) out.cand[o] = s_cand[g];
     if (out.resident) out.resident[o] = res;
@@ -90,13 +108,13 @@ __global__ void __launch_bounds__(kTamThreads)
   }
 }
 
-__global__ void k_tam_adapt(float* __restrict__ lambdas, int layer0, int n, const uint8_t* __restrict__ stall,
+__global__ void k_tam_adapt(float* lambdas, int layer0, int n, const uint8_t* stall,
                             float alpha, float lo, float hi) {
   pdl_launch_dependents();
   pdl_wait();
   const int l = blockIdx.x * blockDim.x + threadIdx.x;
   if (l < n) {
-    const float v = __fadd_rn(lambdas[layer0 + l], stall[l] ? alpha : -alpha);
+    const float v = __fadd_rn(ld_dep(lambdas + layer0 + l), __ldcg(stall + l) ? alpha : -alpha);
     lambdas[layer0 + l] = fminf(hi, fmaxf(lo, v));
   }
 }

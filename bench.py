@@ -198,12 +198,13 @@ def run_ours(args, world, rank, local):
     P = max(1, min(args.tokens, spec.tokens))
     X = W.make_tokens(spec.d, P, seed=args.seed, kind=spec.seq, device=dev).contiguous()  # [P,1,d]
     gw = (spec.n_groups + 31) // 32
-    gmask_all = torch.zeros(nL, gw, dtype=torch.int32, device=dev)
-    masks = []
-    for l in range(nL):
-        m = layers[l].masks(1, device=dev)
-        m.c.gmask = gmask_all[l].data_ptr()
-        masks.append(m)
+    # group masks of all layers, double-buffered by token parity: the momentum
+    # update of token t-1 runs while token t's layers write the other buffer
+    gmask_buf = torch.zeros(2, nL, gw, dtype=torch.int32, device=dev)
+    gmask_all = gmask_buf[0]
+    masks = [layers[l].masks(1, device=dev) for l in range(nL)]
+    side = torch.cuda.Stream(device=dev)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     ws = layers[0].workspace(1, device=dev)
     xa = torch.empty(1, spec.d, device=dev)
     xb = torch.empty(1, spec.d, device=dev)
@@ -215,15 +216,24 @@ def run_ours(args, world, rank, local):
     launches_per_step = nL * 4 + 1 + (1 if spec.anb else 0)
 
     def step(t, xin=None):
+        """Token t through every layer; in parallel, on a side stream, the
+        momentum update (and lambda step) of token t-1, whose group masks sit in
+        the other parity buffer. One momentum update per step."""
+        par = t % 2
+        ev_fork.record(stream)
+        side.wait_event(ev_fork)
+        sffn.tam_update(tam.handle, 0, nL, gmask_buf[1 - par], gw, -1.0, spec.tam_eps, K, outs, side)
+        if spec.anb:
+            sffn.tam_adapt(tam.handle, 0, nL, stalls[(t - 1) % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, side)
+        ev_join.record(side)
         x = X[t % P] if xin is None else xin
         outb = (xa, xb)
         for l in range(nL):
+            masks[l].c.gmask = gmask_buf[par, l].data_ptr()
             xo = outb[l % 2]
             sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
             x = xo
-        sffn.tam_update(tam.handle, 0, nL, gmask_all, gw, -1.0, spec.tam_eps, K, outs, stream)
-        if spec.anb:
-            sffn.tam_adapt(tam.handle, 0, nL, stalls[t % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, stream)
+        stream.wait_event(ev_join)
         return x
 
     # ---- census: active counts per (token, layer); deterministic given the token
@@ -306,6 +316,7 @@ def run_ours(args, world, rank, local):
             for l in range(nL):
                 sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KERNELS],
                                           [ev[k][r][l][1] for k in KERNELS])
+                masks[l].c.gmask = gmask_all[l].data_ptr()
                 xo = outb[l % 2]
                 sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
                 x = xo
