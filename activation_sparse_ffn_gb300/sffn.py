@@ -95,6 +95,7 @@ _sig("sffn_layer_destroy", None, _vp)
 _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
 _sig("sffn_forward", _c, _vp, _vp, _i32, _P(MasksC), _vp, _vp, _vp, _size, _vp)
 _sig("sffn_decode_step", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp, _size, _vp)
+_sig("sffn_decode_step_static_ws", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp)
 _sig("tam_create", _c, _i32, _i32, _f32, _P(_vp))
 _sig("tam_update", _c, _vp, _i32, _i32, _vp, _i32, _f32, _f32, _i32, _P(TamOutputsC), _vp)
 _sig("tam_adapt", _c, _vp, _i32, _i32, _vp, _f32, _f32, _f32, _vp)
@@ -108,7 +109,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_check_error",
-    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "tam_create", "tam_update",
+    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
     "sffn_selftest_wait_timeout",
 ]
@@ -235,6 +236,14 @@ def sffn_forward(layer, x, B, masks: "Masks", y, x_out, ws, stream=None) -> None
 def sffn_decode_step(layer, x, B, thres, masks: "Masks", y, x_out, ws, stream=None) -> None:
     _check(_lib.sffn_decode_step(layer, _ptr(x), B, thres, ctypes.byref(masks.c), _ptr(y), _ptr(x_out), _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)), "sffn_decode_step")
+
+
+def sffn_decode_step_static_ws(layer, x, B, thres, masks: "Masks", y, x_out, stream=None) -> None:
+    """sffn_decode_step without a workspace argument: the scratch lives in a
+    1 MiB device array inside the library, for callers that cannot allocate
+    device memory. Calls sharing a device must not overlap on the GPU."""
+    _check(_lib.sffn_decode_step_static_ws(layer, _ptr(x), B, thres, ctypes.byref(masks.c), _ptr(y), _ptr(x_out),
+                                           _stream(stream)), "sffn_decode_step_static_ws")
 
 
 def sffn_selftest_wait_timeout(layer, limit_us: int, stream=None) -> None:

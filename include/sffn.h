@@ -204,6 +204,23 @@ sffn_status sffn_decode_step(const sffn_layer* layer, const float* x, int32_t B,
                              const sffn_masks* masks, float* y, float* x_out, void* ws,
                              size_t ws_bytes, sffn_stream stream);
 
+/* sffn_decode_step for callers that cannot allocate device memory: a decode
+ * loop that must never stall on an allocation (one can synchronize the whole
+ * GPU), a runtime that reaches this library only through its C ABI and has no
+ * CUDA allocator, or a process whose memory pool refuses new allocations once
+ * serving starts. Same arguments and results as sffn_decode_step, minus the
+ * workspace: scratch comes from one 1 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits. It is
+ * enough for any valid layer at B = 1; a layer/batch needing more returns
+ * INVALID_ARG. The call allocates nothing. Its first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress), so make that first
+ * call before any stream capture. All calls on a device share the array:
+ * calls that can overlap on the GPU race on it and must be ordered by the
+ * caller; nothing in it needs clearing between calls. The pages describe no
+ * counterpart of this call; it exists for callers of this library. */
+sffn_status sffn_decode_step_static_ws(const sffn_layer* layer, const float* x, int32_t B, float thres,
+                                       const sffn_masks* masks, float* y, float* x_out, sffn_stream stream);
+
 /* ---------------------------------------------------------------- TAM */
 
 /* Momentum state for n_layers layers of n_groups groups (1..1024): scores
