@@ -25,26 +25,6 @@ sffn_status invalid(const char* msg) {
   return SFFN_ERR_INVALID_ARG;
 }
 
-// Column slicing of the down projection: as many slices (<= 16) as keep a
-// slice row chunk between 512 bytes and 4 KB and a multiple of 16 bytes.
-bool choose_down_shape(sffn_layer& L) {
-  const int d = L.desc.d, wb = L.wbytes;
-  for (int ns = 16; ns >= 1; ns >>= 1) {
-    if (d % ns) continue;
-    const int W = d / ns;
-    const int bytes = W * wb;
-    if (bytes % 16 || bytes > 4096) continue;
-    if (ns > 1 && bytes < 512) continue;
-    L.down_slices = ns;
-    L.down_width = W;
-    L.down_rows_per_stage = std::min(32, std::max(1, kDownStageBytes / bytes));
-    const int stage = L.down_rows_per_stage * bytes;
-    L.down_stages = std::min(8, std::max(2, kDownSmemBudget / stage));
-    return true;
-  }
-  return false;
-}
-
 sffn_status check_device(int want) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -96,12 +76,8 @@ WsLayout ws_layout(const sffn_layer& L, int B) {
   size_t off = 0;
   w.hid = off;
   off = align256(off + (size_t)B * L.desc.h * 4);
-  w.hval = off;
-  off = align256(off + (size_t)B * L.desc.f * 4);
-  w.alist = off;
-  off = align256(off + (size_t)B * L.desc.f * 4);
-  w.count = off;
-  off = align256(off + (size_t)(B + 1) * 4);
+  w.partials = off;
+  off = align256(off + (size_t)B * ffn_blocks(L) * L.desc.d * 4);
   w.total = off;
   return w;
 }
@@ -156,21 +132,18 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   L->n_groups = desc->f / desc->group_size;
   L->nwords = desc->f / 32;
   L->gwords = (L->n_groups + 31) / 32;
-  if (!choose_down_shape(*L)) {
-    delete L;
-    set_error("no column slicing of d fits the down-projection kernel");
-    return SFFN_ERR_UNSUPPORTED;
-  }
-  {
-    const size_t stage = (size_t)desc->d * L->wbytes * (desc->act == SFFN_ACT_RELU ? 1 : 2);
-    L->up_stages = (int)std::min<size_t>(8, std::max<size_t>(2, kUpSmemBudget / stage));
-    L->score_stages = score_stages_for(*L);
-  }
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
   if (e != cudaSuccess) {
     delete L;
     return cuda_fail(e, "sffn_layer_create: device query");
+  }
+  L->score_stages = score_stages_for(*L);
+  L->ffn_stages = ffn_stages_for(*L);
+  if (L->ffn_stages < 2) {
+    delete L;
+    set_error("sffn_layer_create: the FFN ring does not fit in shared memory for this shape");
+    return SFFN_ERR_UNSUPPORTED;
   }
   const size_t d = desc->d, f = desc->f, h = desc->h, wb = L->wbytes;
   struct {
@@ -326,13 +299,9 @@ sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const s
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout w = ws_layout(*L, B);
   char* base = static_cast<char*>(ws);
-  float* hval = reinterpret_cast<float*>(base + w.hval);
-  int32_t* alist = reinterpret_cast<int32_t*>(base + w.alist);
-  int32_t* cnt = reinterpret_cast<int32_t*>(base + w.count);
-  cudaError_t e = traced(*L, 2, st, [&] {
-    return launch_gather_up(*L, x, m->nmask, nullptr, nullptr, nullptr, hval, alist, cnt, st);
-  });
-  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_down(*L, hval, alist, cnt, x, y, x_out, st); });
+  float* part = reinterpret_cast<float*>(base + w.partials);
+  cudaError_t e = traced(*L, 2, st, [&] { return launch_ffn(*L, x, m->nmask, nullptr, nullptr, nullptr, part, st); });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, x, y, x_out, st); });
   if (e != cudaSuccess) return cuda_fail(e, "sffn_forward: launch");
   return SFFN_OK;
 }
@@ -348,16 +317,14 @@ sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, flo
   const WsLayout w = ws_layout(*L, B);
   char* base = static_cast<char*>(ws);
   float* hid = reinterpret_cast<float*>(base + w.hid);
-  float* hval = reinterpret_cast<float*>(base + w.hval);
-  int32_t* alist = reinterpret_cast<int32_t*>(base + w.alist);
-  int32_t* cnt = reinterpret_cast<int32_t*>(base + w.count);
+  float* part = reinterpret_cast<float*>(base + w.partials);
   cudaError_t e = traced(*L, 0, st, [&] { return launch_pred_hidden(*L, x, hid, st); });
   if (e == cudaSuccess) e = traced(*L, 1, st, [&] { return launch_pred_scores(*L, hid, thres, m->nmask, st); });
   if (e == cudaSuccess)
     e = traced(*L, 2, st, [&] {
-      return launch_gather_up(*L, x, m->nmask, m->idx, m->count, m->gmask, hval, alist, cnt, st);
+      return launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, st);
     });
-  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_down(*L, hval, alist, cnt, x, y, x_out, st); });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, x, y, x_out, st); });
   if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
   return SFFN_OK;
 }

@@ -1,53 +1,53 @@
 // Neuron-aware sparse FFN (PowerInfer §5.3-§5.4): only the rows of up/gate
-// and the transposed-down rows of predicted-active neurons are read.
+// and the transposed-down rows of predicted-active neurons are read, and each
+// thread block owns a disjoint, contiguous slice of the ascending active list
+// (no cross-block synchronisation inside the kernel).
 //
-// k_gather_up: each thread block owns a disjoint, contiguous slice of the
-//   ascending active list (no cross-block synchronisation). Whole up/gate rows
-//   are streamed into a shared-memory ring by one-dimensional bulk copies
-//   (TMA), each thread owns fixed 16-byte chunks of the row so its slice of x
-//   stays in registers, and the activation is fused into the block reduction.
-// k_down: y = sum_i h_i * downT_i. Column slices of d times eight splits of
-//   the active list; each block streams its rows' slice chunks through a ring,
-//   the eight partial sums of a slice are added through distributed shared
-//   memory inside one thread-block cluster, in rank order. No global atomics;
-//   the summation order is fixed, so results are bit-identical run to run.
-#include <cooperative_groups.h>
-
+// k_ffn streams, per block, first the up (and gate) rows of its neurons and
+// then their downT rows through one shared-memory ring of whole-row
+// one-dimensional bulk copies (TMA). Warp 8 is the producer (one lane issues
+// the copies once the eight consumer warps have released a stage through its
+// empty barrier); the consumer warps wait on the stage's full barrier
+// (transaction bytes). Phase A: each consumer thread owns fixed 16-byte chunks
+// of a row, so its slice of x stays in registers; one partial dot product per
+// warp and neuron goes to shared memory. After one barrier among the
+// consumers the partials of every neuron are summed in a fixed order and the
+// activation gives h. Phase B: the same chunk ownership accumulates
+// h_i * downT_i into per-thread registers, so the block ends with a partial of
+// y over its neurons, written to the workspace.
+// k_ffn_reduce adds the blocks' partials in a fixed order (no atomics) and
+// writes y and the residual x + y. Results are bit-identical run to run.
 #include "common.cuh"
 #include "internal.h"
 #include "scan.cuh"
 
-namespace cg = cooperative_groups;
+#include <algorithm>
 
 namespace sffn {
 
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kUpThreads = (kConsumerWarps + 1) * 32;    // 8 consumer warps + 1 producer warp
-constexpr int kDownThreads = (kConsumerWarps + 1) * 32;
+constexpr int kFfnThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
 constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kReduceThreads = 256;
+constexpr int kReduceCols = 32;                          // columns per reduction block
+constexpr int kReduceGroups = kReduceThreads / (kReduceCols / 4);  // 32 partial groups
 
-// Gather of the active up/gate rows. Warp 8 is the producer: one lane issues
-// the bulk copies of neuron k's rows into ring stage k % S once the consumer
-// warps have released that stage (empty barrier, one arrival per warp). The
-// eight consumer warps wait for each stage (full barrier, transaction bytes),
-// form their partial dot products with the x chunks they own, store one
-// partial per warp in shared memory and release the stage; no block-wide
-// barrier inside the loop. After the loop the partials of every neuron are
-// summed in a fixed order and the activation is applied.
+__device__ __forceinline__ void consumer_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
 template <typename T, int ACT, int CPT>
-__global__ void __launch_bounds__(kUpThreads, 1)
-    k_gather_up(const T* __restrict__ up, const T* __restrict__ gate, const float* x,
-                const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages,
-                int list_cap, int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out,
-                uint32_t* __restrict__ gmask_out, float* __restrict__ hval, int32_t* __restrict__ alist,
-                int32_t* __restrict__ ws_count, uint32_t* __restrict__ err) {
-  constexpr int NT = kUpThreads;
+__global__ void __launch_bounds__(kFfnThreads, 1)
+    k_ffn(const T* __restrict__ up, const T* __restrict__ gate, const T* __restrict__ downT, const float* x,
+          const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages, int list_cap,
+          int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, uint32_t* __restrict__ gmask_out,
+          float* __restrict__ partials, uint32_t* __restrict__ err) {
+  constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = ACT != SFFN_ACT_RELU;
+  constexpr int NMAT = GATED ? 2 : 1;  // rows per ring stage in both phases
   const uint32_t row_bytes = (uint32_t)d * sizeof(T);
-  const uint32_t stage_bytes = row_bytes * (GATED ? 2u : 1u);
+  const uint32_t stage_bytes = row_bytes * NMAT;
   const int nch = (int)(row_bytes / 16);
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(kUpThreads, 1)
   uint32_t* s_words = reinterpret_cast<uint32_t*>(empty + stages);
   int* s_off = reinterpret_cast<int*>(s_words + nw);
   int32_t* s_list = reinterpret_cast<int32_t*>(s_off + nw);
-  float* s_part = reinterpret_cast<float*>(s_list + list_cap);  // [list_cap][warps][2]
+  float* s_h = reinterpret_cast<float*>(s_list + list_cap);
+  float* s_part = s_h + list_cap;  // [list_cap][warps][2]
   __shared__ int s_tmp[NT / 32];
   __shared__ int s_abort;
 
@@ -79,360 +80,330 @@ __global__ void __launch_bounds__(kUpThreads, 1)
   const int n_local = min(hi - lo, list_cap);
   extract_slice<NT>(s_words, s_off, nw, lo, lo + n_local, s_list);
   if (b == 0) {
-    if (threadIdx.x == 0) {
-      *ws_count = total;
-      if (count_out) *count_out = total;
-    }
+    if (threadIdx.x == 0 && count_out) *count_out = total;
     if (gmask_out) write_group_mask<NT>(s_words, n_groups, G, gwords, gmask_out);
   }
   __syncthreads();
 
+  const int nA = n_local;                      // phase A units: one neuron (up [+ gate])
+  const int nB = (n_local + NMAT - 1) / NMAT;  // phase B units: NMAT downT rows
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == kConsumerWarps) {
     // ---------------- producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      for (int k = 0; k < n_local; ++k) {
-        const int s = k % stages;
-        const bool ok = k < stages || mbar_wait_bounded(&empty[s], (uint32_t)((k / stages - 1) & 1));
+      for (int u = 0; u < nA + nB; ++u) {
+        const int s = u % stages;
+        const bool ok = u < stages || mbar_wait_bounded(&empty[s], (uint32_t)((u / stages - 1) & 1));
         if (!ok || *(volatile int*)&s_abort) {
           if (!ok) set_device_error(err, SFFN_ERR_TIMEOUT);
           atomicExch(&s_abort, 1);
           // drain: let the copies that may still be in flight land
-          for (int q = max(0, k - stages); q < k; ++q) mbar_wait_bounded(&full[q % stages], (uint32_t)((q / stages) & 1));
+          for (int q = max(0, u - stages); q < u; ++q) mbar_wait_bounded(&full[q % stages], (uint32_t)((q / stages) & 1));
           break;
         }
-        const size_t slot = (size_t)s_list[k];
         unsigned char* dst = ring + (size_t)s * stage_bytes;
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        bulk_g2s(dst, up + slot * d, row_bytes, &full[s], pol);
-        if (GATED) bulk_g2s(dst + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+        if (u < nA) {
+          const size_t slot = (size_t)s_list[u];
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          bulk_g2s(dst, up + slot * d, row_bytes, &full[s], pol);
+          if (GATED) bulk_g2s(dst + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+        } else {
+          const int r0 = (u - nA) * NMAT;
+          const int nr = min(NMAT, n_local - r0);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nr * row_bytes);
+          for (int i = 0; i < nr; ++i)
+            bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s], pol);
+        }
       }
     }
   } else {
-    // ---------------- consumers: this thread's chunks of x, fixed for every row
-    float xr[CPT][EPC];
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const int c = threadIdx.x + j * kConsumers;
-#pragma unroll
-      for (int e = 0; e < EPC; e += 4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < nch) v = ld_dep4(x + (size_t)c * EPC + e);
-        xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
-      }
-    }
-    for (int k = 0; k < n_local; ++k) {
-      const int s = k % stages;
-      // warp-uniform outcome: the shuffles below need every lane
-      const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((k / stages) & 1)));
-      if (!ok) {
-        if (lane == 0) {
-          set_device_error(err, SFFN_ERR_TIMEOUT);
-          atomicExch(&s_abort, 1);
-        }
-        break;
-      }
-      if (__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) break;
-      const unsigned char* sp = ring + (size_t)s * stage_bytes;
-      float pu = 0.f, pg = 0.f;
+    // ---------------- consumers, phase A: partial dot products of up/gate rows
+    {
+      float xr[CPT][EPC];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
         const int c = threadIdx.x + j * kConsumers;
-        if (c < nch) {
-          pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
-          if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+#pragma unroll
+        for (int e = 0; e < EPC; e += 4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (c < nch) v = ld_dep4(x + (size_t)c * EPC + e);
+          xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
         }
       }
-      pu = warp_sum(pu);
-      if (GATED) pg = warp_sum(pg);
-      if (lane == 0) {
-        s_part[((size_t)k * kConsumerWarps + warp) * 2] = pu;
-        s_part[((size_t)k * kConsumerWarps + warp) * 2 + 1] = pg;
+      for (int u = 0; u < nA; ++u) {
+        const int s = u % stages;
+        // warp-uniform outcome: the shuffles below need every lane
+        const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((u / stages) & 1)));
+        if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+          if (!ok && lane == 0) {
+            set_device_error(err, SFFN_ERR_TIMEOUT);
+            atomicExch(&s_abort, 1);
+          }
+          break;
+        }
+        const unsigned char* sp = ring + (size_t)s * stage_bytes;
+        float pu = 0.f, pg = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c = threadIdx.x + j * kConsumers;
+          if (c < nch) {
+            pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
+            if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+          }
+        }
+        pu = warp_sum(pu);
+        if (GATED) pg = warp_sum(pg);
+        if (lane == 0) {
+          s_part[((size_t)u * kConsumerWarps + warp) * 2] = pu;
+          s_part[((size_t)u * kConsumerWarps + warp) * 2 + 1] = pg;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    consumer_barrier();
+    // activation of every local neuron, partials added in warp order
+    for (int a = threadIdx.x; a < nA; a += kConsumers) {
+      float uu = 0.f, gg = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        uu += s_part[((size_t)a * kConsumerWarps + w) * 2];
+        gg += s_part[((size_t)a * kConsumerWarps + w) * 2 + 1];
+      }
+      s_h[a] = neuron_act<ACT>(uu, gg);
+      if (idx_out) idx_out[lo + a] = s_list[a];
+    }
+    consumer_barrier();
+    // ---------------- phase B: acc += h_i * downT_i over this block's neurons
+    float acc[CPT][EPC];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j)
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) acc[j][e] = 0.f;
+    if (!__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+      for (int v = 0; v < nB; ++v) {
+        const int u = nA + v;
+        const int s = u % stages;
+        const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((u / stages) & 1)));
+        if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+          if (!ok && lane == 0) {
+            set_device_error(err, SFFN_ERR_TIMEOUT);
+            atomicExch(&s_abort, 1);
+          }
+          break;
+        }
+        const unsigned char* sp = ring + (size_t)s * stage_bytes;
+        const int r0 = v * NMAT;
+        const int nr = min(NMAT, n_local - r0);
+        for (int i = 0; i < nr; ++i) {
+          const float hv = s_h[r0 + i];
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) {
+            const int c = threadIdx.x + j * kConsumers;
+            if (c < nch) {
+              float w[EPC];
+              WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)i * row_bytes + (size_t)c * 16), w);
+#pragma unroll
+              for (int e = 0; e < EPC; ++e) acc[j][e] = fmaf(hv, w[e], acc[j][e]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+    }
+    // this block's partial of y
+    float* part = partials + (size_t)b * d;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int c = threadIdx.x + j * kConsumers;
+      if (c < nch) {
+#pragma unroll
+        for (int e = 0; e < EPC; e += 4)
+          *reinterpret_cast<float4*>(part + (size_t)c * EPC + e) =
+              make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+      }
     }
   }
   __syncthreads();
-  if (s_abort) return;
-  for (int k = threadIdx.x; k < n_local; k += NT) {
-    float u = 0.f, g = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      u += s_part[((size_t)k * kConsumerWarps + w) * 2];
-      g += s_part[((size_t)k * kConsumerWarps + w) * 2 + 1];
-    }
-    hval[lo + k] = neuron_act<ACT>(u, g);
-    const int sl = s_list[k];
-    alist[lo + k] = sl;
-    if (idx_out) idx_out[lo + k] = sl;
-  }
 }
 
-// Down projection, y = sum_i h_i * downT_i. Thread-block clusters of eight
-// split the active list; the grid's second dimension splits d into column
-// slices. The producer warp streams each row's slice chunk into the ring
-// (one lane per row); the consumer warps accumulate h_i * chunk in registers
-// (each thread owns one 16-byte column chunk and a set of rows) and release
-// stages through the empty barriers. Afterwards the row lanes are summed in
-// shared memory and the eight blocks' partials are added through distributed
-// shared memory in rank order.
-template <typename T>
-__global__ void __launch_bounds__(kDownThreads, 1)
-    k_down(const T* __restrict__ downT, const float* hval, const int32_t* alist,
-           const int32_t* ws_count, const float* x, float* __restrict__ y,
-           float* __restrict__ x_out, int d, int W, int RS, int stages, int list_cap, uint32_t* __restrict__ err) {
-  constexpr int EPC = WType<T>::kPerChunk;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CL = (int)cluster.num_blocks();
-  const int rank = (int)cluster.block_rank();
-  const int slice = blockIdx.y;
-  const uint32_t chunk_bytes = (uint32_t)W * sizeof(T);
-  const int CPR = (int)(chunk_bytes / 16);
-  const int RL = kConsumers / CPR;
-  const int tc = threadIdx.x % CPR, tr = threadIdx.x / CPR;
-  const uint32_t stage_bytes = (uint32_t)RS * chunk_bytes;
-
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + down_region_bytes(W, sizeof(T), RS, stages, kConsumers));
-  uint64_t* empty = full + stages;
-  float* s_h = reinterpret_cast<float*>(empty + stages);     // [list_cap] this block's h values
-  int32_t* s_slot = reinterpret_cast<int32_t*>(s_h + list_cap);  // [list_cap] and their slots
-  __shared__ int s_abort;
-
+// y = sum over blocks of the partials; x_out = x + y. Each block covers
+// kReduceCols columns with kReduceGroups groups of threads, group g adding
+// the partials g, g + kReduceGroups, ... (all loads of a thread issued before
+// any add); the group sums are then added in group order. Fixed order, no
+// atomics.
+template <int PER>
+__global__ void __launch_bounds__(kReduceThreads)
+    k_ffn_reduce(const float* partials, int nparts, int d, const float* x, float* __restrict__ y,
+                 float* __restrict__ x_out) {
   pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    fence_mbar_init();
-    s_abort = 0;
-  }
-  __syncthreads();
-  pdl_wait();  // h values and the active list come from the previous kernel
-
-  const int total = ld_dep(ws_count);
-  const int lo = (int)((long long)total * rank / CL);
-  const int hi = (int)((long long)total * (rank + 1) / CL);
-  const int n_local = min(hi - lo, list_cap);
-  const int nst = (n_local + RS - 1) / RS;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const size_t col0 = (size_t)slice * W;
-  for (int i = threadIdx.x; i < n_local; i += kDownThreads) {
-    s_h[i] = ld_dep(hval + lo + i);
-    s_slot[i] = ld_dep(alist + lo + i);
-  }
-  __syncthreads();
-
-  float acc[EPC];
+  pdl_wait();  // the partials come from the previous kernel
+  constexpr int CG = kReduceCols / 4;             // float4 column groups per block
+  constexpr int GROUPS = kReduceThreads / CG;     // partial groups
+  const int cg = threadIdx.x % CG, pg = threadIdx.x / CG;
+  const int col = blockIdx.x * kReduceCols + cg * 4;
+  __shared__ float4 red[GROUPS][CG];
+  float4 v[PER];
 #pragma unroll
-  for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: stage q = rows [q*RS, q*RS + RS), one lane per row
-    const uint64_t pol = l2_policy_evict_first();
-    for (int q = 0; q < nst; ++q) {
-      const int s = q % stages;
-      const bool ok = __all_sync(SFFN_FULL_MASK, q < stages || mbar_wait_bounded(&empty[s], (uint32_t)((q / stages - 1) & 1)));
-      if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
-        if (lane == 0) {
-          if (!ok) set_device_error(err, SFFN_ERR_TIMEOUT);
-          atomicExch(&s_abort, 1);
-          // drain: let the copies that may still be in flight land
-          for (int r = max(0, q - stages); r < q; ++r) mbar_wait_bounded(&full[r % stages], (uint32_t)((r / stages) & 1));
-        }
-        break;
-      }
-      const int p0 = q * RS;
-      const int nr = min(RS, n_local - p0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nr * chunk_bytes);
-      __syncwarp();
-      if (lane < nr)
-        bulk_g2s(ring + (size_t)s * stage_bytes + (size_t)lane * chunk_bytes, downT + (size_t)s_slot[p0 + lane] * d + col0,
-                 chunk_bytes, &full[s], pol);
-    }
-  } else {
-    // ---------------- consumers
-    for (int q = 0; q < nst; ++q) {
-      const int s = q % stages;
-      const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((q / stages) & 1)));
-      if (!ok) {
-        if (lane == 0) {
-          set_device_error(err, SFFN_ERR_TIMEOUT);
-          atomicExch(&s_abort, 1);
-        }
-        break;
-      }
-      if (__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) break;
-      const int p0 = q * RS;
-      const int nr = min(RS, n_local - p0);
-      if (tr < RL) {
-        const unsigned char* sp = ring + (size_t)s * stage_bytes + (size_t)tc * 16;
-        for (int r = tr; r < nr; r += RL) {
-          const float hv = s_h[p0 + r];
-          float w[EPC];
-          WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)r * chunk_bytes), w);
+  for (int i = 0; i < PER; ++i) {
+    const int p = pg + i * GROUPS;
+    v[i] = (col < d && p < nparts) ? ld_dep4(partials + (size_t)p * d + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float4 acc = v[0];
 #pragma unroll
-          for (int e = 0; e < EPC; ++e) acc[e] = fmaf(hv, w[e], acc[e]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+  for (int i = 1; i < PER; ++i) {
+    acc.x += v[i].x; acc.y += v[i].y; acc.z += v[i].z; acc.w += v[i].w;
+  }
+  red[pg][cg] = acc;
+  __syncthreads();
+  if (threadIdx.x < CG && col < d) {
+    float4 sum = red[0][cg];
+#pragma unroll
+    for (int g = 1; g < GROUPS; ++g) {
+      const float4 w = red[g][cg];
+      sum.x += w.x; sum.y += w.y; sum.z += w.z; sum.w += w.w;
+    }
+    *reinterpret_cast<float4*>(y + col) = sum;
+    if (x_out) {
+      const float4 xv = ld_dep4(x + col);
+      *reinterpret_cast<float4*>(x_out + col) = make_float4(xv.x + sum.x, xv.y + sum.y, xv.z + sum.z, xv.w + sum.w);
     }
   }
-  __syncthreads();
-
-  // per-block partial of this column slice: reduce the row lanes in order
-  // (the ring region is free once every stage has been consumed)
-  float* red = reinterpret_cast<float*>(ring);          // [RL][W]
-  float* part = red + (size_t)RL * W;                   // [W]
-  if (warp < kConsumerWarps && tr < RL) {
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) red[(size_t)tr * W + tc * EPC + e] = acc[e];
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < W; j += kDownThreads) {
-    float sum = 0.f;
-    for (int r = 0; r < RL; ++r) sum += red[(size_t)r * W + j];
-    part[j] = sum;
-  }
-  cluster.sync();
-  // rank r finishes columns [j0, j1) of the slice, adding the partials of
-  // ranks 0..CL-1 in order
-  const int j0 = (int)((long long)W * rank / CL), j1 = (int)((long long)W * (rank + 1) / CL);
-  for (int j = j0 + threadIdx.x; j < j1; j += kDownThreads) {
-    float sum = 0.f;
-    for (int r = 0; r < CL; ++r) sum += cluster.map_shared_rank(part, r)[j];
-    y[col0 + j] = sum;
-    if (x_out) x_out[col0 + j] = ld_dep(x + col0 + j) + sum;
-  }
-  cluster.sync();
 }
 
 template <typename T, int ACT>
-cudaError_t launch_up_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, cudaStream_t st, const float* x,
-                        const uint32_t* nmask, int list_cap, int32_t* idx_out, int32_t* count_out,
-                        uint32_t* gmask_out, float* hval, int32_t* alist, int32_t* ws_count) {
+cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, cudaStream_t st, const float* x,
+                         const uint32_t* nmask, int list_cap, int32_t* idx_out, int32_t* count_out,
+                         uint32_t* gmask_out, float* partials) {
   const T* up = static_cast<const T*>(L.up);
   const T* gate = static_cast<const T*>(L.gate);
-#define SFFN_UP_ARGS                                                                                      \
-  grid, dim3(kUpThreads), smem, st, true, 1, up, gate, x, nmask, L.nwords, L.n_groups, L.desc.group_size, \
-      L.gwords, L.desc.d, L.up_stages, list_cap, idx_out, count_out, gmask_out, hval, alist, ws_count, L.err
+  const T* downT = static_cast<const T*>(L.downT);
+#define SFFN_FFN_ARGS                                                                                         \
+  grid, dim3(kFfnThreads), smem, st, true, 1, up, gate, downT, x, nmask, L.nwords, L.n_groups,                \
+      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err
   switch (cpt) {
-    case 1: return launch_ex(k_gather_up<T, ACT, 1>, SFFN_UP_ARGS);
-    case 2: return launch_ex(k_gather_up<T, ACT, 2>, SFFN_UP_ARGS);
-    case 4: return launch_ex(k_gather_up<T, ACT, 4>, SFFN_UP_ARGS);
-    default: return launch_ex(k_gather_up<T, ACT, 8>, SFFN_UP_ARGS);
+    case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
+    case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);
+    case 4: return launch_ex(k_ffn<T, ACT, 4>, SFFN_FFN_ARGS);
+    default: return launch_ex(k_ffn<T, ACT, 8>, SFFN_FFN_ARGS);
   }
-#undef SFFN_UP_ARGS
+#undef SFFN_FFN_ARGS
+}
+
+template <typename K>
+cudaError_t set_big_smem(K* kern, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 template <typename T, int ACT>
-cudaError_t set_up_attr(size_t smem) {
+cudaError_t set_ffn_attr(size_t smem) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gather_up<T, ACT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gather_up<T, ACT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gather_up<T, ACT, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
-  return cudaFuncSetAttribute(k_gather_up<T, ACT, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if ((e = set_big_smem(k_ffn<T, ACT, 1>, smem))) return e;
+  if ((e = set_big_smem(k_ffn<T, ACT, 2>, smem))) return e;
+  if ((e = set_big_smem(k_ffn<T, ACT, 4>, smem))) return e;
+  return set_big_smem(k_ffn<T, ACT, 8>, smem);
 }
 
-int up_cpt(const sffn_layer& L) {
+int ffn_cpt(const sffn_layer& L) {
   const int nch = L.desc.d * L.wbytes / 16;
   const int need = (nch + kConsumers - 1) / kConsumers;
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
 }
 
-int up_list_cap(const sffn_layer& L) { return (L.desc.f + L.num_sms - 1) / L.num_sms + 1; }
+int ffn_list_cap(const sffn_layer& L) { return (L.desc.f + L.num_sms - 1) / L.num_sms + 1; }
+
+size_t ffn_fixed_smem(const sffn_layer& L) {
+  const size_t cap = (size_t)ffn_list_cap(L);
+  return (size_t)L.nwords * 8 + cap * 4 + cap * 4 + cap * kConsumerWarps * 2 * 4;
+}
 
 }  // namespace
 
-size_t gather_up_smem(const sffn_layer& L) {
-  const size_t row = (size_t)L.desc.d * L.wbytes;
-  const size_t stage = row * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
-  return (size_t)L.up_stages * stage + (size_t)L.up_stages * 16 + (size_t)L.nwords * 8 +
-         (size_t)up_list_cap(L) * 4 + (size_t)up_list_cap(L) * kConsumerWarps * 2 * 4;
+cudaError_t set_max_carveout();
+
+int ffn_blocks(const sffn_layer& L) { return L.num_sms; }
+
+int ffn_stages_for(const sffn_layer& L) {
+  const size_t stage = (size_t)L.desc.d * L.wbytes * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
+  const size_t budget = kFfnSmemBudget > ffn_fixed_smem(L) ? kFfnSmemBudget - ffn_fixed_smem(L) : 0;
+  return (int)std::min<size_t>(kFfnMaxStages, budget / (stage + 16));
 }
 
-int down_list_cap(const sffn_layer& L) { return (L.desc.f + kClusterSplit - 1) / kClusterSplit + 1; }
-
-size_t down_smem(const sffn_layer& L) {
-  return down_region_bytes(L.down_width, L.wbytes, L.down_rows_per_stage, L.down_stages, kConsumers) +
-         (size_t)L.down_stages * 16 + (size_t)down_list_cap(L) * 8;
+size_t ffn_smem(const sffn_layer& L) {
+  const size_t stage = (size_t)L.desc.d * L.wbytes * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
+  return (size_t)L.ffn_stages * (stage + 16) + ffn_fixed_smem(L);
 }
 
 cudaError_t configure_kernels(sffn_layer& L) {
-  const size_t su = gather_up_smem(L), sd = down_smem(L);
-  cudaError_t e = cudaSuccess;
+  const size_t sm = ffn_smem(L);
+  cudaError_t e = set_max_carveout();
+  if (e != cudaSuccess) return e;
   switch (L.desc.wdtype) {
     case SFFN_F32:
-      if ((e = set_up_attr<float, SFFN_ACT_RELU>(su)) || (e = set_up_attr<float, SFFN_ACT_REGLU>(su)) ||
-          (e = set_up_attr<float, SFFN_ACT_SWIGLU>(su)))
-        return e;
-      return cudaFuncSetAttribute(k_down<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
+      if ((e = set_ffn_attr<float, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<float, SFFN_ACT_REGLU>(sm))) return e;
+      return set_ffn_attr<float, SFFN_ACT_SWIGLU>(sm);
     case SFFN_F16:
-      if ((e = set_up_attr<__half, SFFN_ACT_RELU>(su)) || (e = set_up_attr<__half, SFFN_ACT_REGLU>(su)) ||
-          (e = set_up_attr<__half, SFFN_ACT_SWIGLU>(su)))
-        return e;
-      return cudaFuncSetAttribute(k_down<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
+      if ((e = set_ffn_attr<__half, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<__half, SFFN_ACT_REGLU>(sm))) return e;
+      return set_ffn_attr<__half, SFFN_ACT_SWIGLU>(sm);
     default:
-      if ((e = set_up_attr<__nv_bfloat16, SFFN_ACT_RELU>(su)) ||
-          (e = set_up_attr<__nv_bfloat16, SFFN_ACT_REGLU>(su)) ||
-          (e = set_up_attr<__nv_bfloat16, SFFN_ACT_SWIGLU>(su)))
+      if ((e = set_ffn_attr<__nv_bfloat16, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<__nv_bfloat16, SFFN_ACT_REGLU>(sm)))
         return e;
-      return cudaFuncSetAttribute(k_down<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sd);
+      return set_ffn_attr<__nv_bfloat16, SFFN_ACT_SWIGLU>(sm);
   }
 }
 
-cudaError_t launch_gather_up(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
-                             int32_t* count_out, uint32_t* gmask_out, float* hval, int32_t* alist,
-                             int32_t* ws_count, cudaStream_t st) {
-  const dim3 grid(L.num_sms);
-  const size_t smem = gather_up_smem(L);
-  const int cpt = up_cpt(L), cap = up_list_cap(L);
-#define SFFN_UP_DISPATCH(T)                                                                                   \
+
+cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
+                       int32_t* count_out, uint32_t* gmask_out, float* partials, cudaStream_t st) {
+  const dim3 grid(ffn_blocks(L));
+  const size_t smem = ffn_smem(L);
+  const int cpt = ffn_cpt(L), cap = ffn_list_cap(L);
+#define SFFN_FFN_DISPATCH(T)                                                                                  \
   switch (L.desc.act) {                                                                                      \
     case SFFN_ACT_RELU:                                                                                      \
-      return launch_up_t<T, SFFN_ACT_RELU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,         \
-                                           gmask_out, hval, alist, ws_count);                                \
+      return launch_ffn_t<T, SFFN_ACT_RELU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,        \
+                                            gmask_out, partials);                     \
     case SFFN_ACT_REGLU:                                                                                     \
-      return launch_up_t<T, SFFN_ACT_REGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,        \
-                                            gmask_out, hval, alist, ws_count);                               \
+      return launch_ffn_t<T, SFFN_ACT_REGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
+                                             gmask_out, partials);                    \
     default:                                                                                                 \
-      return launch_up_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
-                                             gmask_out, hval, alist, ws_count);                              \
+      return launch_ffn_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,      \
+                                              gmask_out, partials);                   \
   }
   switch (L.desc.wdtype) {
-    case SFFN_F32: SFFN_UP_DISPATCH(float)
-    case SFFN_F16: SFFN_UP_DISPATCH(__half)
-    default: SFFN_UP_DISPATCH(__nv_bfloat16)
+    case SFFN_F32: SFFN_FFN_DISPATCH(float)
+    case SFFN_F16: SFFN_FFN_DISPATCH(__half)
+    default: SFFN_FFN_DISPATCH(__nv_bfloat16)
   }
-#undef SFFN_UP_DISPATCH
+#undef SFFN_FFN_DISPATCH
 }
 
-cudaError_t launch_down(const sffn_layer& L, const float* hval, const int32_t* alist, const int32_t* ws_count,
-                        const float* x, float* y, float* x_out, cudaStream_t st) {
-  const dim3 grid(kClusterSplit, L.down_slices);
-  const size_t smem = down_smem(L);
-#define SFFN_DOWN_ARGS                                                                                     \
-  grid, dim3(kDownThreads), smem, st, true, kClusterSplit, static_cast<const T*>(L.downT), hval, alist,    \
-      ws_count, x, y, x_out, L.desc.d, L.down_width, L.down_rows_per_stage, L.down_stages, down_list_cap(L), L.err
-  switch (L.desc.wdtype) {
-    case SFFN_F32: {
-      using T = float;
-      return launch_ex(k_down<T>, SFFN_DOWN_ARGS);
-    }
-    case SFFN_F16: {
-      using T = __half;
-      return launch_ex(k_down<T>, SFFN_DOWN_ARGS);
-    }
-    default: {
-      using T = __nv_bfloat16;
-      return launch_ex(k_down<T>, SFFN_DOWN_ARGS);
-    }
-  }
-#undef SFFN_DOWN_ARGS
+cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const float* x, float* y, float* x_out,
+                              cudaStream_t st) {
+  const dim3 grid((L.desc.d + kReduceCols - 1) / kReduceCols), block(kReduceThreads);
+  const int nparts = ffn_blocks(L);
+  const int per = (nparts + kReduceGroups - 1) / kReduceGroups;
+  if (per <= 4)
+    return launch_ex(k_ffn_reduce<4>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+  if (per <= 8)
+    return launch_ex(k_ffn_reduce<8>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+  if (per <= 16)
+    return launch_ex(k_ffn_reduce<16>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+  return cudaErrorNotSupported;  // more than 512 blocks: not reached on current GPUs
+}
+
+cudaError_t set_max_carveout() {
+  // Every hot kernel asks for the largest shared-memory carveout, so that
+  // consecutive kernels of a decode step need no L1/shared reconfiguration.
+  cudaError_t e;
+  const int c = cudaSharedmemCarveoutMaxShared;
+  if ((e = cudaFuncSetAttribute(k_ffn_reduce<4>, cudaFuncAttributePreferredSharedMemoryCarveout, c))) return e;
+  if ((e = cudaFuncSetAttribute(k_ffn_reduce<8>, cudaFuncAttributePreferredSharedMemoryCarveout, c))) return e;
+  return cudaFuncSetAttribute(k_ffn_reduce<16>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
 }
 
 }  // namespace sffn

@@ -30,11 +30,7 @@ struct sffn_layer {
   bool has_b1 = false, has_b2 = false;
   // launch shapes chosen at create time
   int score_stages = 0;     // predictor-scores ring depth (one mask word per stage)
-  int up_stages = 0;        // gather-up ring depth
-  int down_slices = 0;      // column slices of the down projection
-  int down_width = 0;       // columns per slice
-  int down_rows_per_stage = 0;
-  int down_stages = 0;
+  int ffn_stages = 0;       // fused FFN ring depth (one neuron's up/gate rows, or as many downT rows)
   // optional timing hooks (sffn_layer_set_trace)
   cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -53,29 +49,14 @@ struct tam_state {
 
 namespace sffn {
 
-constexpr int kClusterSplit = 8;     // thread blocks per cluster in the down projection
-constexpr int kUpSmemBudget = 128 * 1024;
-constexpr int kDownStageBytes = 16 * 1024;
-constexpr int kDownSmemBudget = 80 * 1024;
+constexpr int kFfnSmemBudget = 224 * 1024;
+constexpr int kFfnMaxStages = 12;
 constexpr int kScoreSmemBudget = 192 * 1024;
-
-// Shared memory of the down projection: one region used first as the row
-// ring and then for the per-block column partials ([rows lanes][W] + [W]
-// floats), followed by the stage barriers.
-__host__ __device__ inline size_t down_region_bytes(int W, int wbytes, int rows_per_stage, int stages, int threads) {
-  const size_t ring = (size_t)stages * rows_per_stage * W * wbytes;
-  const int cpr = W * wbytes / 16;
-  const size_t red = ((size_t)(threads / cpr) * W + W) * 4;
-  const size_t r = ring > red ? ring : red;
-  return (r + 15) & ~(size_t)15;
-}
 
 // Workspace of one hot call for batch size B (offsets in bytes, 256-aligned).
 struct WsLayout {
-  size_t hid = 0;     // float [B][h]
-  size_t hval = 0;    // float [B][f]: activation values in active-list order
-  size_t alist = 0;   // int32 [B][f]: active slots, ascending
-  size_t count = 0;   // int32 [B] (+ padding)
+  size_t hid = 0;       // float [B][h]
+  size_t partials = 0;  // float [B][ffn blocks][d]: per-block partial sums of y
   size_t total = 0;
 };
 WsLayout ws_layout(const sffn_layer& L, int B);
@@ -89,11 +70,10 @@ cudaError_t launch_pred_scores(const sffn_layer& L, const float* hid, float thre
                                cudaStream_t st);
 cudaError_t launch_mask_views(const sffn_layer& L, const uint32_t* nmask, int32_t* idx, int32_t* count,
                               uint32_t* gmask, cudaStream_t st);
-cudaError_t launch_gather_up(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
-                             int32_t* count_out, uint32_t* gmask_out, float* hval, int32_t* alist,
-                             int32_t* ws_count, cudaStream_t st);
-cudaError_t launch_down(const sffn_layer& L, const float* hval, const int32_t* alist, const int32_t* ws_count,
-                        const float* x, float* y, float* x_out, cudaStream_t st);
+cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
+                       int32_t* count_out, uint32_t* gmask_out, float* partials, cudaStream_t st);
+cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const float* x, float* y, float* x_out,
+                              cudaStream_t st);
 cudaError_t launch_tam_update(tam_state& S, int layer0, int n_layers, const uint32_t* gmask, int gstride,
                               float lambda, float eps, int K, const tam_outputs& out, cudaStream_t st);
 cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8_t* stall, float alpha,
@@ -110,8 +90,9 @@ cudaError_t configure_kernels(sffn_layer& L);
 cudaError_t configure_predict_kernels(const sffn_layer& L);
 int score_stages_for(const sffn_layer& L);
 size_t score_smem(const sffn_layer& L);
-size_t gather_up_smem(const sffn_layer& L);
-size_t down_smem(const sffn_layer& L);
+int ffn_stages_for(const sffn_layer& L);
+size_t ffn_smem(const sffn_layer& L);
+int ffn_blocks(const sffn_layer& L);
 
 // Launch helper: programmatic dependent launch and optional cluster size.
 template <typename... KArgs, typename... Args>

@@ -8,8 +8,10 @@
 // file-scope device array, so it calls no allocator at all. The caller still
 // owns x, y, x_out and the mask buffers.
 //
-// The array is sized for any valid layer at batch size 1 (every GPU that loads
-// the library holds it until the process exits). All calls on a device share
+// The array holds 16 MiB: the workspace of any valid layer at batch size 1 on
+// a GPU with up to about 240 SMs (the per-block partial sums of y take
+// SMs x d x 4 bytes; at most 10 MB on a 152-SM GB300). Every GPU that loads
+// the library holds it until the process exits. All calls on a device share
 // it: calls that can overlap on the GPU (different streams, or the same array
 // used from two threads without ordering) race on it and must be serialized
 // by the caller. No part of it needs clearing between calls: every scratch
@@ -22,7 +24,7 @@ namespace sffn {
 
 namespace {
 
-constexpr size_t kStaticWsBytes = 1u << 20;  // 1 MiB
+constexpr size_t kStaticWsBytes = 16u << 20;  // 16 MiB
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
@@ -88,7 +90,7 @@ extern "C" sffn_status sffn_decode_step_static_ws(const sffn_layer* L, const flo
   }
   const WsLayout w = ws_layout(*L, B);
   if (w.total > kStaticWsBytes) {
-    set_error("sffn_decode_step_static_ws: this layer needs more scratch than the 1 MiB static array holds; "
+    set_error("sffn_decode_step_static_ws: this layer needs more scratch than the 16 MiB static array holds; "
               "use sffn_decode_step with a caller workspace");
     return SFFN_ERR_INVALID_ARG;
   }
@@ -105,13 +107,11 @@ extern "C" sffn_status sffn_decode_step_static_ws(const sffn_layer* L, const flo
   cudaStream_t st = (cudaStream_t)stream;
   char* base = static_cast<char*>(ws);
   float* hid = reinterpret_cast<float*>(base + w.hid);
-  float* hval = reinterpret_cast<float*>(base + w.hval);
-  int32_t* alist = reinterpret_cast<int32_t*>(base + w.alist);
-  int32_t* cnt = reinterpret_cast<int32_t*>(base + w.count);
+  float* part = reinterpret_cast<float*>(base + w.partials);
   e = launch_pred_hidden(*L, x, hid, st);
   if (e == cudaSuccess) e = launch_pred_scores(*L, hid, thres, m->nmask, st);
-  if (e == cudaSuccess) e = launch_gather_up(*L, x, m->nmask, m->idx, m->count, m->gmask, hval, alist, cnt, st);
-  if (e == cudaSuccess) e = launch_down(*L, hval, alist, cnt, x, y, x_out, st);
+  if (e == cudaSuccess) e = launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, st);
+  if (e == cudaSuccess) e = launch_ffn_reduce(*L, part, x, y, x_out, st);
   if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step_static_ws: launch");
   return SFFN_OK;
 }

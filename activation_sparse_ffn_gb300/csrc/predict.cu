@@ -250,12 +250,31 @@ size_t score_smem(const sffn_layer& L) {
   return (size_t)L.score_stages * 32 * L.desc.h * L.wbytes + (size_t)L.score_stages * 8 + (size_t)L.desc.h * 4;
 }
 
+template <typename K>
+cudaError_t carveout_max(K* kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
+template <typename T>
+cudaError_t configure_predict_t(int sm) {
+  // every hot kernel asks for the largest shared-memory carveout, so that
+  // consecutive kernels of a decode step need no L1/shared reconfiguration
+  cudaError_t e = cudaFuncSetAttribute(k_pred_scores<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  if (e == cudaSuccess) e = carveout_max(k_pred_scores<T>);
+  if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 1>);
+  if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 2>);
+  if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 4>);
+  if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 8>);
+  if (e == cudaSuccess) e = carveout_max(k_mask_views);
+  return e;
+}
+
 cudaError_t configure_predict_kernels(const sffn_layer& L) {
   const int sm = (int)score_smem(L);
   switch (L.desc.wdtype) {
-    case SFFN_F32: return cudaFuncSetAttribute(k_pred_scores<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    case SFFN_F16: return cudaFuncSetAttribute(k_pred_scores<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    default: return cudaFuncSetAttribute(k_pred_scores<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    case SFFN_F32: return configure_predict_t<float>(sm);
+    case SFFN_F16: return configure_predict_t<__half>(sm);
+    default: return configure_predict_t<__nv_bfloat16>(sm);
   }
 }
 

@@ -191,7 +191,7 @@ def sffn_layer_packed(layer) -> PackedView:
     return out
 
 
-TRACE_KERNELS = ("pred_hidden", "pred_scores", "gather_up", "down")
+TRACE_KERNELS = ("pred_hidden", "pred_scores", "ffn", "ffn_reduce")
 
 
 def sffn_layer_set_trace(layer, begin=None, end=None) -> None:
@@ -240,7 +240,7 @@ def sffn_decode_step(layer, x, B, thres, masks: "Masks", y, x_out, ws, stream=No
 
 def sffn_decode_step_static_ws(layer, x, B, thres, masks: "Masks", y, x_out, stream=None) -> None:
     """sffn_decode_step without a workspace argument: the scratch lives in a
-    1 MiB device array inside the library, for callers that cannot allocate
+    16 MiB device array inside the library, for callers that cannot allocate
     device memory. Calls sharing a device must not overlap on the GPU."""
     _check(_lib.sffn_decode_step_static_ws(layer, _ptr(x), B, thres, ctypes.byref(masks.c), _ptr(y), _ptr(x_out),
                                            _stream(stream)), "sffn_decode_step_static_ws")

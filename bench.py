@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 DEFAULT_WORKLOAD = "llama2_70b_reglu_d8192_f28672_bf16_8l"
 METRIC = "sparse-FFN decode tokens/s at B=1; active-byte HBM GB/s as % of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS = ("pred_hidden", "pred_scores", "gather_up", "down")
+KERNELS = ("pred_hidden", "pred_scores", "ffn", "ffn_reduce")
 
 
 def parse_args():
@@ -138,12 +138,13 @@ def layer_bytes(spec, count: int, with_b2: bool) -> dict:
     """Algorithmic bytes of one layer-token, per kernel: the weight rows the
     method must read plus the small vectors each kernel must move."""
     d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
-    nmat_up = 1 if spec.act == "relu" else 2
     k = {
         "pred_hidden": h * d * wb + d * 4 + h * 4,
         "pred_scores": f * h * wb + h * 4 + f // 8 + (f * 4 if with_b2 else 0),
-        "gather_up": count * nmat_up * d * wb + d * 4 + f // 8 + count * 8,
-        "down": count * d * wb + count * 8 + 3 * d * 4,
+        # active up/gate/down rows + x + mask words (the per-block partials stay in L2)
+        "ffn": count * spec.n_mats * d * wb + d * 4 + f // 8,
+        # x read, y and x + y written (partials read from L2 are not HBM traffic)
+        "ffn_reduce": 3 * d * 4,
     }
     # the metric: predictor weights + all rows of active neurons + x + y
     metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + count * spec.n_mats * d * wb + 2 * d * 4

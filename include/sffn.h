@@ -161,8 +161,9 @@ sffn_status sffn_layer_check_error(const sffn_layer* layer, sffn_stream stream);
 void sffn_layer_destroy(sffn_layer* layer);
 
 /* Optional per-kernel timing hooks. Kernel slots: 0 predictor hidden layer,
- * 1 predictor scores + threshold, 2 gather of up/gate rows + activation,
- * 3 down projection. When set, every later hot call on this layer records
+ * 1 predictor scores + threshold, 2 sparse FFN (gather of active up/gate rows,
+ * activation, and the active downT rows into per-block partial sums),
+ * 3 reduction of the partial sums into y (and x + y). When set, every later hot call on this layer records
  * begin[k] on its stream right before launching kernel k and end[k] right
  * after it (NULL entries are skipped). The handles are cudaEvent_t values owned
  * by the caller, which must keep them alive while tracing is on. Recording
@@ -209,10 +210,10 @@ sffn_status sffn_decode_step(const sffn_layer* layer, const float* x, int32_t B,
  * GPU), a runtime that reaches this library only through its C ABI and has no
  * CUDA allocator, or a process whose memory pool refuses new allocations once
  * serving starts. Same arguments and results as sffn_decode_step, minus the
- * workspace: scratch comes from one 1 MiB device array inside the library,
+ * workspace: scratch comes from one 16 MiB device array inside the library,
  * which every GPU that loads the library holds until the process exits. It is
- * enough for any valid layer at B = 1; a layer/batch needing more returns
- * INVALID_ARG. The call allocates nothing. Its first call on each device looks
+ * enough for any valid layer at B = 1 on a GPU with up to about 240 SMs; a
+ * layer/batch needing more returns INVALID_ARG. The call allocates nothing. Its first call on each device looks
  * up the array's device address (cudaGetSymbolAddress), so make that first
  * call before any stream capture. All calls on a device share the array:
  * calls that can overlap on the GPU race on it and must be ordered by the
