@@ -33,17 +33,22 @@ sffn_status check_device(int want) {
   return SFFN_OK;
 }
 
+size_t ws_bytes_for(const sffn_layer& L, int B) {
+  return B == 1 ? ws_layout(L, 1).total : batch_ws_layout(L, B).total;
+}
+
 sffn_status check_ws(const sffn_layer* L, int B, const void* ws, size_t ws_bytes) {
   if (!ws) return invalid("ws is NULL");
   if (!aligned(ws, 256)) return invalid("ws must be 256-byte aligned");
-  if (ws_bytes < ws_layout(*L, B).total) return invalid("ws_bytes is smaller than sffn_workspace_bytes(layer, B)");
+  if (ws_bytes < ws_bytes_for(*L, B)) return invalid("ws_bytes is smaller than sffn_workspace_bytes(layer, B)");
   return SFFN_OK;
 }
 
 sffn_status check_batch(const sffn_layer* L, int B) {
   if (B < 1 || B > L->desc.max_batch) return invalid("B must be in [1, max_batch]");
-  if (B > 1) {
-    set_error("batch sizes above 1 are not implemented in this build");
+  std::string why;
+  if (B > 1 && !batch_supported(*L, &why)) {
+    set_error(why);
     return SFFN_ERR_UNSUPPORTED;
   }
   return SFFN_OK;
@@ -172,6 +177,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   e = cudaMemset(L->err, 0, 256);
   if (e == cudaSuccess) e = configure_kernels(*L);
   if (e == cudaSuccess) e = configure_predict_kernels(*L);
+  if (e == cudaSuccess) e = configure_batch_kernels(*L);
   if (e != cudaSuccess) {
     rc = cuda_fail(e, "sffn_layer_create: kernel set-up");
     sffn_layer_destroy(L);
@@ -226,7 +232,7 @@ sffn_status sffn_layer_set_trace(sffn_layer* L, const sffn_trace* t) {
 
 size_t sffn_workspace_bytes(const sffn_layer* L, int32_t B) {
   if (!L || B < 1 || B > L->desc.max_batch) return 0;
-  return ws_layout(*L, B).total;
+  return ws_bytes_for(*L, B);
 }
 
 static sffn_status read_error_word(uint32_t* err, cudaStream_t st) {
@@ -279,6 +285,11 @@ sffn_status sffn_predict(const sffn_layer* L, const float* x, int32_t B, float t
   sffn_status rc = check_hot(L, x, B, m, ws, ws_bytes);
   if (rc != SFFN_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
+  if (B > 1) {
+    cudaError_t e = launch_batch(*L, x, B, thres, m, true, false, nullptr, nullptr, ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sffn_predict: launch");
+    return SFFN_OK;
+  }
   const WsLayout w = ws_layout(*L, B);
   float* hid = reinterpret_cast<float*>(static_cast<char*>(ws) + w.hid);
   cudaError_t e = traced(*L, 0, st, [&] { return launch_pred_hidden(*L, x, hid, st); });
@@ -297,6 +308,11 @@ sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const s
   if (y == x) return invalid("y must not alias x");
   if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
   cudaStream_t st = (cudaStream_t)stream;
+  if (B > 1) {
+    cudaError_t e = launch_batch(*L, x, B, 0.f, m, false, true, y, x_out, ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sffn_forward: launch");
+    return SFFN_OK;
+  }
   const WsLayout w = ws_layout(*L, B);
   char* base = static_cast<char*>(ws);
   float* part = reinterpret_cast<float*>(base + w.partials);
@@ -314,6 +330,11 @@ sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, flo
   if (y == x) return invalid("y must not alias x");
   if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
   cudaStream_t st = (cudaStream_t)stream;
+  if (B > 1) {
+    cudaError_t e = launch_batch(*L, x, B, thres, m, true, true, y, x_out, ws, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
+    return SFFN_OK;
+  }
   const WsLayout w = ws_layout(*L, B);
   char* base = static_cast<char*>(ws);
   float* hid = reinterpret_cast<float*>(base + w.hid);

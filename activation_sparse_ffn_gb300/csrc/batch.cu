@@ -1,0 +1,648 @@
+// Batched decode (B > 1): the union of the batch's predicted masks decides
+// which FFN rows are read, each token keeps its own mask for its own output
+// (KAIROX 问题与动机: larger batches raise the number of activated neurons;
+// PowerInfer §5.3-§5.4 neuron-aware operators). Every contraction of a batch
+// step is a tall-skinny product (many weight rows, N = 16 or 32 tokens) run
+// on the fifth-generation tensor cores:
+//   hidden  D[h x N]  = W1 [contiguous rows, K = d]          . X^T
+//   scores  D[f x N]  = W2 [contiguous rows, K = h]          . HID^T
+//   up/gate D[U x N]  = up, gate [union rows, K = d]         . X^T
+//   down    D[d x N]  = downT^T [K = union rows, MN-major A] . H^T
+// by one persistent kernel (k_tc_gemm) that writes fp32 partial products
+// over K splits; small CUDA-core kernels finish each step (bias, ReLU,
+// threshold + ballot, activation with the per-token mask, residual).
+// Activations enter the tensor cores as a high and a low 16-bit part
+// (v = hi + lo, two MMAs accumulating into the same fp32 tile), which keeps
+// their product with the 16-bit weights close to fp32 accuracy.
+#include "common.cuh"
+#include "internal.h"
+#include "scan.cuh"
+#include "tcgen05.cuh"
+
+#include <algorithm>
+#include <string>
+
+namespace sffn {
+
+namespace {
+
+constexpr int kGemmThreads = 256;    // warps 0-3 producers, warp 4 MMA issuer, warps 4-7 epilogue
+constexpr int kProducers = 128;
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int kGemmSmemBudget = 200 * 1024;
+constexpr int kViewThreadsB = 1024;
+
+struct GemmArgs {
+  const unsigned char* A0;  // first A matrix
+  const unsigned char* A1;  // second A matrix with the same rows (gate), or null
+  const int32_t* rows;      // gathered rows of A (null: row i is row i)
+  const int32_t* count_dev; // device extent of the row-indexed dimension (null: fixed_count)
+  int fixed_count;
+  int other;                // K-major: K extent; MN-major: M extent (elements, multiple of 64 / 128)
+  int lda;                  // elements per A row
+  const unsigned char* Bhl; // [2][npad][ldb] 16-bit hi then lo parts, K-major
+  int ldb;
+  float* D;                 // partials [ks][m_tiles * 128][npad]
+  size_t dmat_stride;       // floats from the first matrix's partials to the second's
+  int target_units;
+  uint32_t* err;
+};
+
+// Work decomposition shared by the GEMM and its finishers.
+struct Plan {
+  int m_tiles, kblocks, ks, units;
+};
+
+__host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, int target) {
+  Plan p;
+  if (!mn_major) {
+    p.m_tiles = (count + kTileM - 1) / kTileM;
+    p.kblocks = other / kTileK;
+  } else {
+    p.m_tiles = other / kTileM;
+    p.kblocks = (count + kTileK - 1) / kTileK;
+  }
+  if (p.m_tiles == 0 || p.kblocks == 0) {
+    p.ks = 0;
+    p.units = 0;
+    return p;
+  }
+  int ks = (target + p.m_tiles - 1) / p.m_tiles;
+  ks = ks < 1 ? 1 : (ks > p.kblocks ? p.kblocks : ks);
+  p.ks = ks;
+  p.units = p.m_tiles * ks;
+  return p;
+}
+
+template <bool MN, int NMAT, int NPAD>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf16, int stages) {
+  constexpr uint32_t kA = kTileM * kTileK * 2;   // 16 KB per A tile
+  constexpr uint32_t kB = NPAD * kTileK * 2;     // one B part (hi or lo)
+  constexpr uint32_t kStage = NMAT * kA + 2 * kB;
+  constexpr uint32_t kCols = (NMAT * NPAD) <= 32 ? 32u : ((NMAT * NPAD) <= 64 ? 64u : 128u);
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * kStage);
+  uint64_t* empty = full + stages;
+  uint64_t* dfull = empty + stages;
+  uint64_t* dempty = dfull + 1;
+  uint64_t* drain = dempty + 1;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], kProducers);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(dempty, 4);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 4) tc::alloc(&s_tmem, kCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+
+  pdl_launch_dependents();
+  pdl_wait();  // operands and row lists come from earlier kernels
+  const int count = g.count_dev ? ld_dep(g.count_dev) : g.fixed_count;
+  const Plan p = make_plan(MN, count, g.other, g.target_units);
+  const size_t mrows = (size_t)p.m_tiles * kTileM;
+
+  auto krange = [&](int kq, int& kb0, int& kb1) {
+    kb0 = (int)((long long)p.kblocks * kq / p.ks);
+    kb1 = (int)((long long)p.kblocks * (kq + 1) / p.ks);
+  };
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ producers
+    int it = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const int mt = u / p.ks, kq = u % p.ks;
+      int kb0, kb1;
+      krange(kq, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % stages;
+        const bool ok = __all_sync(SFFN_FULL_MASK,
+                                   it < stages || mbar_wait_bounded(&empty[s], (uint32_t)((it / stages - 1) & 1)));
+        if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+          if (!ok && lane == 0) {
+            set_device_error(g.err, SFFN_ERR_TIMEOUT);
+            atomicExch(&s_abort, 1);
+          }
+          goto producers_done;
+        }
+        unsigned char* st = ring + (size_t)s * kStage;
+        if (!MN) {
+          // thread t copies row t of the 128-row tile: 8 chunks per matrix
+          const int m = mt * kTileM + tid;
+          const int r = m < count ? (g.rows ? ld_dep(g.rows + m) : m) : 0;
+          const size_t src = ((size_t)r * g.lda + (size_t)kb * kTileK) * 2;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            tc::cp_async16(st + tc::kmajor_off(tid, j), g.A0 + src + j * 16);
+            if (NMAT == 2) tc::cp_async16(st + kA + tc::kmajor_off(tid, j), g.A1 + src + j * 16);
+          }
+        } else {
+          // thread t copies half (64 M elements) of K row t/2 of the tile
+          const int k = tid >> 1, half = tid & 1;
+          const int kidx = kb * kTileK + k;
+          const int r = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
+          const size_t src = ((size_t)r * g.lda + (size_t)mt * kTileM + half * 64) * 2;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tc::cp_async16(st + tc::mnmajor_off(k, half * 8 + c), g.A0 + src + c * 16);
+        }
+        // B: hi and lo parts, NPAD rows x 8 chunks each
+        unsigned char* sb = st + NMAT * kA;
+#pragma unroll
+        for (int idx = tid; idx < 2 * NPAD * 8; idx += kProducers) {
+          const int hl = idx / (NPAD * 8), n = (idx / 8) % NPAD, j = idx % 8;
+          tc::cp_async16(sb + hl * kB + tc::kmajor_off(n, j),
+                         g.Bhl + (((size_t)hl * NPAD + n) * g.ldb + (size_t)kb * kTileK + j * 8) * 2);
+        }
+        tc::cp_async_arrive(&full[s]);
+      }
+    }
+  producers_done:
+    tc::cp_async_wait_all();
+  } else {
+    // ------------------------------------------------- MMA issue + epilogue
+    const uint32_t idesc = tc::instr_desc(bf16, MN, NPAD);
+    const int ew = warp - 4;  // TMEM lane quarter of this warp
+    int it = 0, ui = 0;
+    bool issued = false;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++ui) {
+      const int mt = u / p.ks, kq = u % p.ks;
+      int kb0, kb1;
+      krange(kq, kb0, kb1);
+      if (warp == 4 && lane == 0) {
+        bool ok = ui == 0 || mbar_wait_bounded(dempty, (uint32_t)((ui - 1) & 1));
+        if (ok) tc::fence_after();
+        for (int kb = kb0; ok && kb < kb1; ++kb, ++it) {
+          const int s = it % stages;
+          ok = mbar_wait_bounded(&full[s], (uint32_t)((it / stages) & 1));
+          if (!ok || *(volatile int*)&s_abort) break;
+          fence_proxy_async_smem();  // cp.async writes -> tensor core reads
+          tc::fence_after();
+          const uint32_t sa = smem_u32(ring + (size_t)s * kStage);
+          const uint32_t sb = sa + NMAT * kA;
+#pragma unroll
+          for (int step = 0; step < 4; ++step) {
+#pragma unroll
+            for (int a = 0; a < NMAT; ++a) {
+              const uint64_t ad = MN ? tc::smem_desc(sa + step * 4096, 1024, 2048)
+                                     : tc::smem_desc(sa + a * kA + step * 32, 16, 1024);
+#pragma unroll
+              for (int hl = 0; hl < 2; ++hl) {
+                const uint64_t bd = tc::smem_desc(sb + hl * kB + step * 32, 16, 1024);
+                tc::mma(tmem + a * NPAD, ad, bd, idesc, !(kb == kb0 && step == 0 && hl == 0));
+              }
+            }
+          }
+          tc::commit(&empty[s]);
+          issued = true;
+        }
+        if (!ok) {
+          set_device_error(g.err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        tc::commit(dfull);
+        issued = true;
+      }
+      __syncwarp();
+      // epilogue: every warp of 4..7 reads its 32 rows of each accumulator
+      const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(dfull, (uint32_t)(ui & 1)));
+      if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+        if (!ok && lane == 0) {
+          set_device_error(g.err, SFFN_ERR_TIMEOUT);
+          atomicExch(&s_abort, 1);
+        }
+        break;
+      }
+      tc::fence_after();
+      const size_t row = (size_t)mt * kTileM + ew * 32 + lane;
+#pragma unroll
+      for (int a = 0; a < NMAT; ++a) {
+        float* dst = g.D + (size_t)a * g.dmat_stride + ((size_t)kq * mrows + row) * NPAD;
+#pragma unroll
+        for (int c0 = 0; c0 < NPAD; c0 += 16) {
+          float v[16];
+          tc::ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * NPAD + c0), v);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);
+    }
+    // let every issued MMA finish before tensor memory is released
+    if (warp == 4 && lane == 0 && issued) {
+      tc::commit(drain);
+      mbar_wait_bounded(drain, 0u);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 4) tc::dealloc(tmem, kCols);
+}
+
+// ---------------------------------------------------------------- finishers
+
+template <typename T>
+__device__ __forceinline__ void split16(float v, T& hi, T& lo);
+
+template <>
+__device__ __forceinline__ void split16<__nv_bfloat16>(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+template <>
+__device__ __forceinline__ void split16<__half>(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+
+// out[hl][n][k] for n < npad, k < K: hi/lo parts of in[n][k] (n < B), zero rows n >= B.
+template <typename T>
+__global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const size_t total = (size_t)npad * K;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(i / K);
+    const float v = n < B ? ld_dep(in + i) : 0.f;
+    T hi, lo;
+    split16<T>(v, hi, lo);
+    out[i] = hi;
+    out[total + i] = lo;
+  }
+}
+
+// hid[n][j] = ReLU(sum_kq D[kq][j][n] + b1[j]) as hi/lo parts [2][npad][h].
+template <typename T>
+__global__ void k_b_hidden_fin(const float* D, int ks, int mrows, int npad, int h, int B, const float* b1, T* out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = n * h + j
+  if (i >= npad * h) return;
+  const int n = i / h, j = i % h;
+  float v = 0.f;
+  if (n < B) {
+    float s = 0.f;
+    for (int kq = 0; kq < ks; ++kq) s += ld_dep(D + ((size_t)kq * mrows + j) * npad + n);
+    if (b1) s += b1[j];
+    v = relu_nan(s);
+  }
+  T hi, lo;
+  split16<T>(v, hi, lo);
+  out[i] = hi;
+  out[(size_t)npad * h + i] = lo;
+}
+
+// nmask[n][w] for every token n < B: one warp per mask word, one ballot per token.
+__global__ void k_b_scores_fin(const float* D, int ks, int mrows, int npad, int nw, int B, const float* b2,
+                               float thres, uint32_t* nmask) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= nw) return;
+  const int row = w * 32 + lane;
+  const float bias = b2 ? b2[row] : 0.f;
+  uint32_t mine = 0;
+  for (int n = 0; n < B; ++n) {
+    float s = 0.f;
+    for (int kq = 0; kq < ks; ++kq) s += ld_dep(D + ((size_t)kq * mrows + row) * npad + n);
+    s += bias;
+    const uint32_t m = __ballot_sync(SFFN_FULL_MASK, s >= thres);  // NaN compares false
+    if (lane == n) mine = m;
+  }
+  if (lane < B) nmask[(size_t)lane * nw + w] = mine;
+}
+
+// Views: block b < B expands token b's mask (index list, count, group mask);
+// block B forms the union mask (OR over tokens) and its views.
+__global__ void __launch_bounds__(kViewThreadsB)
+    k_b_views(const uint32_t* nmask, int B, int nw, int f, int n_groups, int G, int gwords, int32_t* idx,
+              int32_t* count, uint32_t* gmask, uint32_t* unmask, int32_t* uidx, int32_t* ucount, uint32_t* ugmask) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(smem);
+  int* s_off = reinterpret_cast<int*>(s_words + nw);
+  __shared__ int s_tmp[kViewThreadsB / 32];
+  const int b = blockIdx.x;
+  const uint32_t* src;
+  if (b < B) {
+    src = nmask + (size_t)b * nw;
+  } else {
+    // union words into the union mask output, then scanned like any token
+    for (int w = threadIdx.x; w < nw; w += kViewThreadsB) {
+      uint32_t m = 0;
+      for (int n = 0; n < B; ++n) m |= ld_dep(nmask + (size_t)n * nw + w);
+      unmask[w] = m;
+    }
+    __syncthreads();
+    __threadfence_block();
+    src = unmask;
+  }
+  const int total = scan_mask_words<kViewThreadsB>(src, nw, s_words, s_off, s_tmp);
+  if (b < B) {
+    if (idx) extract_slice<kViewThreadsB>(s_words, s_off, nw, 0, total, idx + (size_t)b * f);
+    if (count && threadIdx.x == 0) count[b] = total;
+    if (gmask) write_group_mask<kViewThreadsB>(s_words, n_groups, G, gwords, gmask + (size_t)b * gwords);
+  } else {
+    extract_slice<kViewThreadsB>(s_words, s_off, nw, 0, total, uidx);
+    if (threadIdx.x == 0) *ucount = total;
+    if (ugmask) write_group_mask<kViewThreadsB>(s_words, n_groups, G, gwords, ugmask);
+  }
+}
+
+// H parts [2][npad][ldh]: h = act(g, u) for union neuron i and token n if the
+// neuron is in token n's own mask, else 0; zero beyond the union and for n >= B.
+template <typename T, int ACT>
+__global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32_t* ucount,
+                            const int32_t* uidx, const uint32_t* nmask, int nw, int npad, int B, int ldh,
+                            int target, T* H) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int U = ld_dep(ucount);
+  const Plan p = make_plan(false, U, d, target);  // the up/gate product's plan (K = d)
+  const size_t total = (size_t)npad * ldh;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(i / ldh), u = (int)(i % ldh);
+    float v = 0.f;
+    if (n < B && u < U) {
+      const int slot = ld_dep(uidx + u);
+      if ((ld_dep(nmask + (size_t)n * nw + (slot >> 5)) >> (slot & 31)) & 1u) {
+        const size_t mrows = (size_t)p.m_tiles * kTileM;
+        float uu = 0.f, gg = 0.f;
+        for (int kq = 0; kq < p.ks; ++kq) {
+          uu += ld_dep(Du + ((size_t)kq * mrows + u) * npad + n);
+          if (ACT != SFFN_ACT_RELU) gg += ld_dep(Dg + ((size_t)kq * mrows + u) * npad + n);
+        }
+        v = neuron_act<ACT>(uu, gg);
+      }
+    }
+    T hi, lo;
+    split16<T>(v, hi, lo);
+    H[i] = hi;
+    H[total + i] = lo;
+  }
+}
+
+// y[n][c] = sum_kq D[kq][c][n]; x_out = x + y.
+__global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad, int B, int target, const float* x,
+                          float* y, float* x_out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int U = ld_dep(ucount);
+  const Plan p = make_plan(true, U, d, target);
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = n * d + c
+  if (i >= B * d) return;
+  const int n = i / d, c = i % d;
+  float s = 0.f;
+  for (int kq = 0; kq < p.ks; ++kq) s += ld_dep(D + ((size_t)kq * d + c) * npad + n);
+  y[i] = s;
+  if (x_out) x_out[i] = ld_dep(x + i) + s;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+int npad_of(int B) { return B <= 16 ? 16 : 32; }
+int gemm_target(const sffn_layer& L) { return 2 * L.num_sms; }
+
+size_t rows_bound(const sffn_layer& L, int m_tiles_max) {
+  return ((size_t)gemm_target(L) + (size_t)m_tiles_max) * kTileM;
+}
+
+template <bool MN, int NMAT, int NPAD>
+size_t gemm_smem(int stages) {
+  const size_t stage = (size_t)NMAT * kTileM * kTileK * 2 + 2 * (size_t)NPAD * kTileK * 2;
+  return 1024 + (size_t)stages * stage + (size_t)(2 * stages + 3) * 8;
+}
+
+template <bool MN, int NMAT, int NPAD>
+int gemm_stages() {
+  const size_t stage = (size_t)NMAT * kTileM * kTileK * 2 + 2 * (size_t)NPAD * kTileK * 2;
+  return (int)std::min<size_t>(8, (kGemmSmemBudget - 2048) / stage);
+}
+
+template <bool MN, int NMAT, int NPAD>
+cudaError_t set_gemm_attr() {
+  const size_t smem = gemm_smem<MN, NMAT, NPAD>(gemm_stages<MN, NMAT, NPAD>());
+  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<MN, NMAT, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_tc_gemm<MN, NMAT, NPAD>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+template <bool MN, int NMAT, int NPAD>
+cudaError_t launch_gemm(const sffn_layer& L, const GemmArgs& g, cudaStream_t st) {
+  const int stages = gemm_stages<MN, NMAT, NPAD>();
+  const size_t smem = gemm_smem<MN, NMAT, NPAD>(stages);
+  return launch_ex(k_tc_gemm<MN, NMAT, NPAD>, dim3(L.num_sms), dim3(kGemmThreads), smem, st, true, 1, g,
+                   L.desc.wdtype == SFFN_BF16, stages);
+}
+
+template <bool MN, int NMAT>
+cudaError_t launch_gemm_n(const sffn_layer& L, int npad, const GemmArgs& g, cudaStream_t st) {
+  return npad == 16 ? launch_gemm<MN, NMAT, 16>(L, g, st) : launch_gemm<MN, NMAT, 32>(L, g, st);
+}
+
+}  // namespace
+
+BatchWs batch_ws_layout(const sffn_layer& L, int B) {
+  BatchWs w;
+  const int npad = 32;  // sized for the largest padding
+  const size_t d = L.desc.d, f = L.desc.f, h = L.desc.h;
+  const size_t fpad = (f + kTileK - 1) / kTileK * kTileK;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = (off + bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  (void)B;
+  w.xhl = take(2 * npad * d * 2);
+  w.dh = take(rows_bound(L, (int)((h + kTileM - 1) / kTileM)) * npad * 4);
+  w.hidhl = take(2 * npad * h * 2);
+  w.ds = take(rows_bound(L, (int)((f + kTileM - 1) / kTileM)) * npad * 4);
+  w.unmask = take((f / 32) * 4);
+  w.uidx = take(f * 4);
+  w.ucount = take(256);
+  w.dug = take(2 * rows_bound(L, (int)((f + kTileM - 1) / kTileM)) * npad * 4);
+  w.hhl = take(2 * npad * fpad * 2);
+  w.dy = take(rows_bound(L, (int)(d / kTileM)) * npad * 4);
+  w.total = off;
+  return w;
+}
+
+bool batch_supported(const sffn_layer& L, std::string* why) {
+  if (L.desc.wdtype == SFFN_F32) {
+    if (why) *why = "batched calls need 16-bit weights (fp16 or bf16)";
+    return false;
+  }
+  if (L.desc.d % kTileM || L.desc.h % kTileK) {
+    if (why) *why = "batched calls need d a multiple of 128 and h a multiple of 64";
+    return false;
+  }
+  return true;
+}
+
+cudaError_t configure_batch_kernels(const sffn_layer& L) {
+  if (!batch_supported(L, nullptr)) return cudaSuccess;
+  cudaError_t e;
+  if ((e = set_gemm_attr<false, 1, 16>())) return e;
+  if ((e = set_gemm_attr<false, 1, 32>())) return e;
+  if ((e = set_gemm_attr<false, 2, 16>())) return e;
+  if ((e = set_gemm_attr<false, 2, 32>())) return e;
+  if ((e = set_gemm_attr<true, 1, 16>())) return e;
+  return set_gemm_attr<true, 1, 32>();
+}
+
+cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
+                         bool forward, float* y, float* x_out, void* ws, cudaStream_t st) {
+  const BatchWs w = batch_ws_layout(L, B);
+  char* base = static_cast<char*>(ws);
+  const int npad = npad_of(B);
+  const int d = L.desc.d, f = L.desc.f, h = L.desc.h, nw = L.nwords;
+  const int fpad = (f + kTileK - 1) / kTileK * kTileK;
+  const bool bf = L.desc.wdtype == SFFN_BF16;
+  const int target = gemm_target(L);
+  uint32_t* unmask = m->unmask ? m->unmask : reinterpret_cast<uint32_t*>(base + w.unmask);
+  int32_t* uidx = m->uidx ? m->uidx : reinterpret_cast<int32_t*>(base + w.uidx);
+  int32_t* ucount = m->ucount ? m->ucount : reinterpret_cast<int32_t*>(base + w.ucount);
+  cudaError_t e = cudaSuccess;
+  // x -> hi/lo parts [2][npad][d]
+  void* xhl = base + w.xhl;
+  const int split_blocks = std::min(1024, (npad * d + 255) / 256);
+  if (bf)
+    e = launch_ex(k_b_split<__nv_bfloat16>, dim3(split_blocks), dim3(256), 0, st, true, 1, x, B, d, npad,
+                  static_cast<__nv_bfloat16*>(xhl));
+  else
+    e = launch_ex(k_b_split<__half>, dim3(split_blocks), dim3(256), 0, st, true, 1, x, B, d, npad,
+                  static_cast<__half*>(xhl));
+  if (e != cudaSuccess) return e;
+
+  if (predict) {
+    // hidden: D[h x N] = W1 . X^T over K = d
+    GemmArgs g{};
+    g.A0 = static_cast<const unsigned char*>(L.W1);
+    g.fixed_count = h;
+    g.other = d;
+    g.lda = d;
+    g.Bhl = static_cast<const unsigned char*>(xhl);
+    g.ldb = d;
+    g.D = reinterpret_cast<float*>(base + w.dh);
+    g.target_units = target;
+    g.err = L.err;
+    e = launch_gemm_n<false, 1>(L, npad, g, st);
+    if (e != cudaSuccess) return e;
+    const Plan ph = make_plan(false, h, d, target);
+    void* hidhl = base + w.hidhl;
+    const int hb = (npad * h + 255) / 256;
+    const float* b1 = L.has_b1 ? L.b1 : nullptr;
+    if (bf)
+      e = launch_ex(k_b_hidden_fin<__nv_bfloat16>, dim3(hb), dim3(256), 0, st, true, 1,
+                    static_cast<const float*>(g.D), ph.ks, ph.m_tiles * kTileM, npad, h, B, b1,
+                    static_cast<__nv_bfloat16*>(hidhl));
+    else
+      e = launch_ex(k_b_hidden_fin<__half>, dim3(hb), dim3(256), 0, st, true, 1, static_cast<const float*>(g.D),
+                    ph.ks, ph.m_tiles * kTileM, npad, h, B, b1, static_cast<__half*>(hidhl));
+    if (e != cudaSuccess) return e;
+    // scores: D[f x N] = W2 . HID^T over K = h
+    GemmArgs s{};
+    s.A0 = static_cast<const unsigned char*>(L.W2);
+    s.fixed_count = f;
+    s.other = h;
+    s.lda = h;
+    s.Bhl = static_cast<const unsigned char*>(hidhl);
+    s.ldb = h;
+    s.D = reinterpret_cast<float*>(base + w.ds);
+    s.target_units = target;
+    s.err = L.err;
+    e = launch_gemm_n<false, 1>(L, npad, s, st);
+    if (e != cudaSuccess) return e;
+    const Plan ps = make_plan(false, f, h, target);
+    const float* b2 = L.has_b2 ? L.b2 : nullptr;
+    e = launch_ex(k_b_scores_fin, dim3((nw + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
+                  ps.ks, ps.m_tiles * kTileM, npad, nw, B, b2, thres, m->nmask);
+    if (e != cudaSuccess) return e;
+  }
+  // per-token views (when predicting) and the union mask with its views
+  e = launch_ex(k_b_views, dim3(B + 1), dim3(kViewThreadsB), (size_t)nw * 8, st, true, 1,
+                static_cast<const uint32_t*>(m->nmask), B, nw, f, L.n_groups, L.desc.group_size, L.gwords,
+                predict ? m->idx : nullptr, predict ? m->count : nullptr, predict ? m->gmask : nullptr, unmask, uidx,
+                ucount, m->ugmask);
+  if (e != cudaSuccess || !forward) return e;
+
+  // up/gate over the union rows: D[U x N] = {up, gate} . X^T over K = d
+  const bool gated = L.desc.act != SFFN_ACT_RELU;
+  const size_t dmat = rows_bound(L, (f + kTileM - 1) / kTileM) * npad;
+  GemmArgs u{};
+  u.A0 = static_cast<const unsigned char*>(L.up);
+  u.A1 = gated ? static_cast<const unsigned char*>(L.gate) : nullptr;
+  u.rows = uidx;
+  u.count_dev = ucount;
+  u.other = d;
+  u.lda = d;
+  u.Bhl = static_cast<const unsigned char*>(xhl);
+  u.ldb = d;
+  u.D = reinterpret_cast<float*>(base + w.dug);
+  u.dmat_stride = dmat;
+  u.target_units = target;
+  u.err = L.err;
+  e = gated ? launch_gemm_n<false, 2>(L, npad, u, st) : launch_gemm_n<false, 1>(L, npad, u, st);
+  if (e != cudaSuccess) return e;
+  // activation with each token's own mask -> H parts [2][npad][fpad]
+  void* hhl = base + w.hhl;
+  const int ab = std::min(2048, (npad * fpad + 255) / 256);
+#define SFFN_ACT_LAUNCH(T, A)                                                                                     \
+  launch_ex(k_b_act_fin<T, A>, dim3(ab), dim3(256), 0, st, true, 1, static_cast<const float*>(u.D),              \
+            static_cast<const float*>(u.D + dmat), d, static_cast<const int32_t*>(ucount),                        \
+            static_cast<const int32_t*>(uidx), static_cast<const uint32_t*>(m->nmask), nw, npad, B, fpad, target, \
+            static_cast<T*>(hhl))
+  switch (L.desc.act) {
+    case SFFN_ACT_RELU: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_RELU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_RELU); break;
+    case SFFN_ACT_REGLU: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_REGLU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_REGLU); break;
+    default: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_SWIGLU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_SWIGLU); break;
+  }
+#undef SFFN_ACT_LAUNCH
+  if (e != cudaSuccess) return e;
+  // down: D[d x N] = downT^T (MN-major, K = union rows) . H^T
+  GemmArgs dn{};
+  dn.A0 = static_cast<const unsigned char*>(L.downT);
+  dn.rows = uidx;
+  dn.count_dev = ucount;
+  dn.other = d;
+  dn.lda = d;
+  dn.Bhl = static_cast<const unsigned char*>(hhl);
+  dn.ldb = fpad;
+  dn.D = reinterpret_cast<float*>(base + w.dy);
+  dn.target_units = target;
+  dn.err = L.err;
+  e = launch_gemm_n<true, 1>(L, npad, dn, st);
+  if (e != cudaSuccess) return e;
+  return launch_ex(k_b_y_fin, dim3((B * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
+                   static_cast<const int32_t*>(ucount), d, npad, B, target, x, y, x_out);
+}
+
+}  // namespace sffn

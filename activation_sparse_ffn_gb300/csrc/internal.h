@@ -61,6 +61,17 @@ struct WsLayout {
 };
 WsLayout ws_layout(const sffn_layer& L, int B);
 
+// Workspace of a batched call (B > 1), offsets in bytes.
+struct BatchWs {
+  size_t xhl = 0, dh = 0, hidhl = 0, ds = 0, unmask = 0, uidx = 0, ucount = 0, dug = 0, hhl = 0, dy = 0, total = 0;
+};
+BatchWs batch_ws_layout(const sffn_layer& L, int B);
+bool batch_supported(const sffn_layer& L, std::string* why);
+cudaError_t configure_batch_kernels(const sffn_layer& L);
+// Batched predictor (predict) and/or sparse FFN over the union (forward).
+cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
+                         bool forward, float* y, float* x_out, void* ws, cudaStream_t st);
+
 void set_error(const std::string& msg);
 sffn_status cuda_fail(cudaError_t e, const char* what);
 

@@ -336,13 +336,13 @@ def test_timeout_path_reports_and_recovers(sffn):
     _token_check(L, host, "relu", "f16", 32, x, 0.0, masks, y)
 
 
-def test_batch_above_one_is_reported_unsupported(sffn):
-    spec = W.LayerSpec(name="t", d=64, f=64, h=8, group_size=32, act="relu", wdtype="f16", p_mean=0.2,
+def test_batch_above_one_needs_16bit_weights(sffn):
+    spec = W.LayerSpec(name="t", d=64, f=64, h=8, group_size=32, act="relu", wdtype="f32", p_mean=0.2,
                        zipf_alpha=1.0)
     w = W.make_layer(spec, seed=0, device="cuda")
     L = sffn.Layer.from_weights(w, 32, "relu", max_batch=4)
     x = torch.zeros(4, 64, device="cuda")
     y = torch.empty(4, 64, device="cuda")
     with pytest.raises(sffn.SffnError) as e:
-        sffn.sffn_decode_step(L.handle, x, 4, 0.0, L.masks(4), y, None, L.workspace(4))
+        sffn.sffn_decode_step(L.handle, x, 4, 0.0, L.masks(4), y, None, L.workspace(1))
     assert e.value.status == sffn.SFFN_ERR_UNSUPPORTED
