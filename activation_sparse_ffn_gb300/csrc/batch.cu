@@ -518,6 +518,16 @@ cudaError_t configure_batch_kernels(const sffn_layer& L) {
   return set_gemm_attr<true, 1, 32>();
 }
 
+// Records the layer's trace event for slot k (if any) around `launch`.
+template <typename F>
+cudaError_t traced_b(const sffn_layer& L, int k, cudaStream_t st, F&& launch) {
+  cudaError_t e = cudaSuccess;
+  if (L.trace_begin[k]) e = cudaEventRecord(L.trace_begin[k], st);
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess && L.trace_end[k]) e = cudaEventRecord(L.trace_end[k], st);
+  return e;
+}
+
 cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
                          bool forward, float* y, float* x_out, void* ws, cudaStream_t st) {
   const BatchWs w = batch_ws_layout(L, B);
@@ -554,7 +564,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     g.D = reinterpret_cast<float*>(base + w.dh);
     g.target_units = target;
     g.err = L.err;
-    e = launch_gemm_n<false, 1>(L, npad, g, st);
+    e = traced_b(L, 0, st, [&] { return launch_gemm_n<false, 1>(L, npad, g, st); });
     if (e != cudaSuccess) return e;
     const Plan ph = make_plan(false, h, d, target);
     void* hidhl = base + w.hidhl;
@@ -579,7 +589,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     s.D = reinterpret_cast<float*>(base + w.ds);
     s.target_units = target;
     s.err = L.err;
-    e = launch_gemm_n<false, 1>(L, npad, s, st);
+    e = traced_b(L, 1, st, [&] { return launch_gemm_n<false, 1>(L, npad, s, st); });
     if (e != cudaSuccess) return e;
     const Plan ps = make_plan(false, f, h, target);
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
@@ -610,7 +620,9 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   u.dmat_stride = dmat;
   u.target_units = target;
   u.err = L.err;
-  e = gated ? launch_gemm_n<false, 2>(L, npad, u, st) : launch_gemm_n<false, 1>(L, npad, u, st);
+  e = traced_b(L, 2, st, [&] {
+    return gated ? launch_gemm_n<false, 2>(L, npad, u, st) : launch_gemm_n<false, 1>(L, npad, u, st);
+  });
   if (e != cudaSuccess) return e;
   // activation with each token's own mask -> H parts [2][npad][fpad]
   void* hhl = base + w.hhl;
@@ -639,7 +651,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.D = reinterpret_cast<float*>(base + w.dy);
   dn.target_units = target;
   dn.err = L.err;
-  e = launch_gemm_n<true, 1>(L, npad, dn, st);
+  e = traced_b(L, 3, st, [&] { return launch_gemm_n<true, 1>(L, npad, dn, st); });
   if (e != cudaSuccess) return e;
   return launch_ex(k_b_y_fin, dim3((B * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
                    static_cast<const int32_t*>(ucount), d, npad, B, target, x, y, x_out);

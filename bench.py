@@ -35,6 +35,8 @@ DEFAULT_WORKLOAD = "llama2_70b_reglu_d8192_f28672_bf16_8l"
 METRIC = "sparse-FFN decode tokens/s at B=1; active-byte HBM GB/s as % of GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 KERNELS = ("pred_hidden", "pred_scores", "ffn", "ffn_reduce")
+KERNELS_BATCH = ("hidden_gemm", "scores_gemm", "upgate_gemm", "down_gemm")
+BF16_PEAK_KEY = "bf16_tflops"
 
 
 def parse_args():
@@ -46,6 +48,7 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--layers", type=int, default=0, help="override the number of layers (0 = the workload's)")
+    p.add_argument("--batch", type=int, default=1, help="tokens per decode step (independent streams)")
     p.add_argument("--tokens", type=int, default=128, help="distinct tokens cycled through (one graph each)")
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     p.add_argument("--profile-steps", type=int, default=64)
@@ -71,6 +74,15 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)[BF16_PEAK_KEY]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -134,6 +146,31 @@ def _num(s):
 
 # ----------------------------------------------------------------------------- bytes
 
+def batch_layer_cost(spec, ucount: int, B: int, with_b2: bool) -> dict:
+    """Algorithmic bytes of one layer and batch step (predictor weights once,
+    every union row once, x and y of every token) and the tensor-core work
+    executed per product (128-row tiles, N padded to 16/32, two MMAs per
+    product for the hi/lo parts of the activations)."""
+    d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
+    nmat_up = 1 if spec.act == "relu" else 2
+    npad = 16 if B <= 16 else 32
+    tiles = lambda m: -(-m // 128) * 128
+    k = {
+        "hidden_gemm": h * d * wb,
+        "scores_gemm": f * h * wb + (f * 4 if with_b2 else 0),
+        "upgate_gemm": ucount * nmat_up * d * wb,
+        "down_gemm": ucount * d * wb,
+    }
+    flops = {
+        "hidden_gemm": 2 * 2 * tiles(h) * npad * d,
+        "scores_gemm": 2 * 2 * tiles(f) * npad * h,
+        "upgate_gemm": 2 * 2 * nmat_up * tiles(ucount) * npad * d,
+        "down_gemm": 2 * 2 * d * npad * (-(-ucount // 64) * 64),
+    }
+    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + ucount * spec.n_mats * d * wb + 2 * B * d * 4
+    return {"kernels": k, "flops": flops, "metric": metric}
+
+
 def layer_bytes(spec, count: int, with_b2: bool) -> dict:
     """Algorithmic bytes of one layer-token, per kernel: the weight rows the
     method must read plus the small vectors each kernel must move."""
@@ -172,8 +209,14 @@ def run_ours(args, world, rank, local):
     from activation_sparse_ffn_gb300 import workload as W
 
     spec = W.WORKLOADS[args.workload]
+    Bt = max(1, args.batch)
+    replicas_note = None
     if args.layers:
         spec = W.spec_replace(spec, layers=args.layers)
+    elif spec.layers == 1:
+        # a single layer is rotated over 4 replicas so that L2 never holds a step's rows
+        spec = W.spec_replace(spec, layers=4)
+        replicas_note = "single-layer workload rotated over 4 independent layer replicas"
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     nL = spec.layers
@@ -184,7 +227,7 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         for l in range(nL):
             w = W.make_layer(spec, seed=args.seed, layer=l, device=dev)
-            layers.append(sffn.Layer.from_weights(w, spec.group_size, spec.act, max_batch=1, stream=stream))
+            layers.append(sffn.Layer.from_weights(w, spec.group_size, spec.act, max_batch=Bt, stream=stream))
             if l == 0 and want_cpu:
                 host0 = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v)
                          for k, v in w.items()}
@@ -197,24 +240,34 @@ def run_ours(args, world, rank, local):
 
     # ---- buffers
     P = max(1, min(args.tokens, spec.tokens))
-    X = W.make_tokens(spec.d, P, seed=args.seed, kind=spec.seq, device=dev).contiguous()  # [P,1,d]
+    X = W.make_tokens(spec.d, P, seed=args.seed, kind=spec.seq, batch=Bt, device=dev).contiguous()  # [P,B,d]
     gw = (spec.n_groups + 31) // 32
     # group masks of all layers, double-buffered by token parity: the momentum
     # update of token t-1 runs while token t's layers write the other buffer
     gmask_buf = torch.zeros(2, nL, gw, dtype=torch.int32, device=dev)
     gmask_all = gmask_buf[0]
-    masks = [layers[l].masks(1, device=dev) for l in range(nL)]
+    masks = [layers[l].masks(Bt, device=dev) for l in range(nL)]
     side = torch.cuda.Stream(device=dev)
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
-    ws = layers[0].workspace(1, device=dev)
-    xa = torch.empty(1, spec.d, device=dev)
-    xb = torch.empty(1, spec.d, device=dev)
-    ybuf = torch.empty(1, spec.d, device=dev)
+
+    def set_tam_mask(l, ptr):
+        # the momentum update reads the token's group mask (B = 1) or the batch union's
+        if Bt == 1:
+            masks[l].c.gmask = ptr
+        else:
+            masks[l].c.ugmask = ptr
+    ws = layers[0].workspace(Bt, device=dev)
+    xa = torch.empty(Bt, spec.d, device=dev)
+    xb = torch.empty(Bt, spec.d, device=dev)
+    ybuf = torch.empty(Bt, spec.d, device=dev)
     tam = sffn.Tam(nL, spec.n_groups, spec.tam_lambda)
     K = spec.capacity
     outs = sffn.TamOutputs(nL, spec.n_groups, K, device=dev)
     stalls = torch.from_numpy(W.make_stall_bits(P, nL, seed=args.seed)).to(dev) if spec.anb else None
-    launches_per_step = nL * 4 + 1 + (1 if spec.anb else 0)
+    # B = 1: hidden, scores, fused FFN, reduction. B > 1: split of x, hidden
+    # product + finisher, scores product + finisher, mask views, up/gate
+    # product + activation, down product + finisher.
+    launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0)
 
     def step(t, xin=None):
         """Token t through every layer; in parallel, on a side stream, the
@@ -230,23 +283,32 @@ def run_ours(args, world, rank, local):
         x = X[t % P] if xin is None else xin
         outb = (xa, xb)
         for l in range(nL):
-            masks[l].c.gmask = gmask_buf[par, l].data_ptr()
+            set_tam_mask(l, gmask_buf[par, l].data_ptr())
             xo = outb[l % 2]
-            sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
+            sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
             x = xo
         stream.wait_event(ev_join)
         return x
 
     # ---- census: active counts per (token, layer); deterministic given the token
-    counts = np.zeros((P, nL), dtype=np.int64)
+    counts = np.zeros((P, nL), dtype=np.int64)       # active (B = 1) or union (B > 1) neurons
+    tok_counts = np.zeros((P, nL), dtype=np.int64)   # sum over tokens of their own active neurons
     with torch.cuda.stream(stream):
         for t in range(P):
             step(t)
-            counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
+            if Bt == 1:
+                counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
+                tok_counts[t] = counts[t]
+            else:
+                counts[t] = torch.stack([m.ucount[0] for m in masks]).cpu().numpy()
+                tok_counts[t] = torch.stack([m.count.sum() for m in masks]).cpu().numpy()
     for L in layers:
         L.check_error(stream)
-    metric_bytes = np.array([[layer_bytes(spec, int(counts[t, l]), with_b2)["metric"] for l in range(nL)]
-                             for t in range(P)]).sum(axis=1)
+
+    def cost(c):
+        return layer_bytes(spec, c, with_b2) if Bt == 1 else batch_layer_cost(spec, c, Bt, with_b2)
+
+    metric_bytes = np.array([[cost(int(counts[t, l]))["metric"] for l in range(nL)] for t in range(P)]).sum(axis=1)
 
     # ---- graphs: one per distinct token
     graphs = None
@@ -301,25 +363,26 @@ def run_ours(args, world, rank, local):
     toks = [(t_start + i) % P for i in range(args.steps)]
     timed_bytes = float(sum(metric_bytes[t] for t in toks))
     sec = elapsed_ms / 1e3
-    value = world * args.steps / sec
+    value = world * Bt * args.steps / sec
     ms_per_step = elapsed_ms / args.steps
     step_gbs = timed_bytes / sec / 1e9
 
     # ---- traced pass: per-kernel durations (events around each kernel)
     R = min(args.profile_steps, P)
+    KN = KERNELS if Bt == 1 else KERNELS_BATCH
     ev = {k: [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
-              for _ in range(R)] for k in KERNELS}
+              for _ in range(R)] for k in KN}
     tam_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
     with torch.cuda.stream(stream):
         for r in range(R):
             x = X[r % P]
             outb = (xa, xb)
             for l in range(nL):
-                sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KERNELS],
-                                          [ev[k][r][l][1] for k in KERNELS])
-                masks[l].c.gmask = gmask_all[l].data_ptr()
+                sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KN],
+                                          [ev[k][r][l][1] for k in KN])
+                set_tam_mask(l, gmask_all[l].data_ptr())
                 xo = outb[l % 2]
-                sffn.sffn_decode_step(layers[l].handle, x, 1, spec.thres, masks[l], ybuf, xo, ws, stream)
+                sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
                 x = xo
             tam_ev[r][0].record(stream)
             sffn.tam_update(tam.handle, 0, nL, gmask_all, gw, -1.0, spec.tam_eps, K, outs, stream)
@@ -328,24 +391,27 @@ def run_ours(args, world, rank, local):
     for L in layers:
         sffn.sffn_layer_set_trace(L.handle)
     per_kernel = {}
-    for k in KERNELS:
+    for k in KN:
         durs = [ev[k][r][l][0].elapsed_time(ev[k][r][l][1]) for r in range(R) for l in range(nL)]
-        kb = [layer_bytes(spec, int(counts[r % P, l]), with_b2)["kernels"][k] for r in range(R) for l in range(nL)]
+        kb = [cost(int(counts[r % P, l]))["kernels"][k] for r in range(R) for l in range(nL)]
         per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
                          "gbs": sum(kb) / (sum(durs) / 1e3) / 1e9}
+        if Bt > 1:
+            kf = [cost(int(counts[r % P, l]))["flops"][k] for r in range(R) for l in range(nL)]
+            per_kernel[k]["tflops"] = sum(kf) / (sum(durs) / 1e3) / 1e12
     tam_us = 1e3 * sum(a.elapsed_time(b) for a, b in tam_ev) / R
-    dom = max(KERNELS, key=lambda k: per_kernel[k]["us"])
+    dom = max(KN, key=lambda k: per_kernel[k]["us"])
 
     # ---- dense run of the same layer: every neuron active (thres = -inf)
     dense_us = None
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for i in range(3):
-            sffn.sffn_decode_step(layers[0].handle, X[i % P], 1, float("-inf"), masks[0], ybuf, xa, ws, stream)
+            sffn.sffn_decode_step(layers[0].handle, X[i % P], Bt, float("-inf"), masks[0], ybuf, xa, ws, stream)
         e0.record(stream)
         nd = 20
         for i in range(nd):
-            sffn.sffn_decode_step(layers[i % nL].handle, X[i % P], 1, float("-inf"), masks[i % nL], ybuf, xa, ws,
+            sffn.sffn_decode_step(layers[i % nL].handle, X[i % P], Bt, float("-inf"), masks[i % nL], ybuf, xa, ws,
                                   stream)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -353,8 +419,8 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end through the public API with host buffers
     Xh = X.cpu().pin_memory()
-    xin = torch.empty(1, spec.d, device=dev)
-    yh = torch.empty(1, spec.d).pin_memory()
+    xin = torch.empty(Bt, spec.d, device=dev)
+    yh = torch.empty(Bt, spec.d).pin_memory()
     g_e2e = None
     if graphs is not None:
         g_e2e = torch.cuda.CUDAGraph()
@@ -376,17 +442,18 @@ def run_ours(args, world, rank, local):
             yh.copy_(out, non_blocking=True)
             stream.synchronize()
     e2e_sec = time.perf_counter() - t0
-    e2e_value = world * E / e2e_sec
+    e2e_value = world * Bt * E / e2e_sec
 
     # ---- CPU baseline: the oracle on layer 0, as it stands
     cpu = None
     if want_cpu and host0 is not None:
         cpu = cpu_baseline(spec, host0, X[:, 0].double().cpu().numpy(), args.cpu_seconds)
+        cpu["sample"] += "; one token at a time (a batch costs its tokens' sum)" if Bt > 1 else ""
 
     peak, peak_kind = measured_peaks()
     pk = per_kernel[dom]
     dom_traffic = None
-    active_frac = float(counts.mean() / spec.f)
+    active_frac = float(tok_counts.mean() / Bt / spec.f)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -401,7 +468,7 @@ def run_ours(args, world, rank, local):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": nL, "batch": 1,
+            "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": nL, "batch": Bt,
             "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype, "thres": spec.thres,
             "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
             "distinct_tokens": P, "graphs": graphs is not None,
@@ -419,12 +486,20 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(pk["gbs"], 1), "peak": peak,
                      "unit": "GB/s", "frac": round(pk["gbs"] / peak, 4), "traffic": dom_traffic,
                      "peak_kind": peak_kind},
-        "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": spec.d * 4,
-                "d2h_bytes_per_step": spec.d * 4, "steps": E, "sync_per_step": True},
+        "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": Bt * spec.d * 4,
+                "d2h_bytes_per_step": Bt * spec.d * 4, "steps": E, "sync_per_step": True},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if replicas_note:
+        line["config"]["replicas"] = replicas_note
+    if Bt > 1:
+        line["union_frac"] = round(float(counts.mean() / spec.f), 5)
+        tpk, _ = measured_tensor_peak()
+        line["kernels_tflops"] = {k: round(v["tflops"], 2) for k, v in per_kernel.items()}
+        line["tensor"] = {"kernel": dom, "achieved_tflops": round(pk["tflops"], 2), "peak": tpk,
+                          "frac": round(pk["tflops"] / tpk, 5), "note": "executed MMA work incl. padding and hi/lo"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -160,10 +160,12 @@ sffn_status sffn_layer_check_error(const sffn_layer* layer, sffn_stream stream);
 
 void sffn_layer_destroy(sffn_layer* layer);
 
-/* Optional per-kernel timing hooks. Kernel slots: 0 predictor hidden layer,
- * 1 predictor scores + threshold, 2 sparse FFN (gather of active up/gate rows,
- * activation, and the active downT rows into per-block partial sums),
- * 3 reduction of the partial sums into y (and x + y). When set, every later hot call on this layer records
+/* Optional per-kernel timing hooks. Kernel slots for B = 1: 0 predictor
+ * hidden layer, 1 predictor scores + threshold, 2 sparse FFN (gather of active
+ * up/gate rows, activation, and the active downT rows into per-block partial
+ * sums), 3 reduction of the partial sums into y (and x + y). For B > 1 the
+ * slots time the four tensor-core products: 0 hidden, 1 scores, 2 up/gate
+ * over the union rows, 3 down over the union rows. When set, every later hot call on this layer records
  * begin[k] on its stream right before launching kernel k and end[k] right
  * after it (NULL entries are skipped). The handles are cudaEvent_t values owned
  * by the caller, which must keep them alive while tracing is on. Recording
