@@ -123,12 +123,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers
+    // Each warp-wide copy instruction covers whole 128-byte lines. K-major:
+    // eight threads per row, thread t copies 16-byte chunk t & 7 of tile rows
+    // (t >> 3) + 16i. MN-major: sixteen threads per K row, thread t copies
+    // chunk t & 15 of the tile's 256 bytes of M in K rows (t >> 4) + 8i.
+    const int j8 = tid & 7, r8 = tid >> 3;
+    const int c16 = tid & 15, k16 = tid >> 4;
     int it = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const int mt = u / p.ks, kq = u % p.ks;
       int kb0, kb1;
       krange(kq, kb0, kb1);
+      // K-major: byte offsets of this thread's eight rows, fixed over the unit.
+      size_t roff[8];
+      // MN-major: the warp's gathered rows for eight stages, four per lane:
+      // lane l holds in ridx[q] the row of stage 2q + (l >> 4), K row
+      // 2 * warp + (l & 1) + 8 * ((l >> 1) & 7) of that stage.
+      int ridx[4] = {0, 0, 0, 0};
+      if (!MN) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int m = mt * kTileM + r8 + 16 * i;
+          const int r = m < count ? (g.rows ? ld_dep(g.rows + m) : m) : 0;
+          roff[i] = (size_t)r * g.lda * 2 + (size_t)j8 * 16;
+        }
+      }
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        if (MN && ((kb - kb0) & 7) == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kidx = (kb + 2 * q + (lane >> 4)) * kTileK + 2 * warp + (lane & 1) + 8 * ((lane >> 1) & 7);
+            ridx[q] = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
+          }
+        }
         const int s = it % stages;
         const bool ok = __all_sync(SFFN_FULL_MASK,
                                    it < stages || mbar_wait_bounded(&empty[s], (uint32_t)((it / stages - 1) & 1)));
@@ -141,23 +168,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
         }
         unsigned char* st = ring + (size_t)s * kStage;
         if (!MN) {
-          // thread t copies row t of the 128-row tile: 8 chunks per matrix
-          const int m = mt * kTileM + tid;
-          const int r = m < count ? (g.rows ? ld_dep(g.rows + m) : m) : 0;
-          const size_t src = ((size_t)r * g.lda + (size_t)kb * kTileK) * 2;
+          const size_t kofs = (size_t)kb * kTileK * 2;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            tc::cp_async16(st + tc::kmajor_off(tid, j), g.A0 + src + j * 16);
-            if (NMAT == 2) tc::cp_async16(st + kA + tc::kmajor_off(tid, j), g.A1 + src + j * 16);
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t so = tc::kmajor_off(r8 + 16 * i, j8);
+            tc::cp_async16(st + so, g.A0 + roff[i] + kofs);
+            if (NMAT == 2) tc::cp_async16(st + kA + so, g.A1 + roff[i] + kofs);
           }
         } else {
-          // thread t copies half (64 M elements) of K row t/2 of the tile
-          const int k = tid >> 1, half = tid & 1;
-          const int kidx = kb * kTileK + k;
-          const int r = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
-          const size_t src = ((size_t)r * g.lda + (size_t)mt * kTileM + half * 64) * 2;
+          const int sc = (kb - kb0) & 7;  // stage within the eight held in ridx
+          const int q = sc >> 1;
+          const int v = q == 0 ? ridx[0] : (q == 1 ? ridx[1] : (q == 2 ? ridx[2] : ridx[3]));
+          const size_t mofs = ((size_t)mt * kTileM + c16 * 8) * 2;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) tc::cp_async16(st + tc::mnmajor_off(k, half * 8 + c), g.A0 + src + c * 16);
+          for (int i = 0; i < 8; ++i) {
+            const int r = __shfl_sync(SFFN_FULL_MASK, v, ((sc & 1) << 4) | (i << 1) | (lane >> 4));
+            tc::cp_async16(st + tc::mnmajor_off(k16 + 8 * i, c16), g.A0 + (size_t)r * g.lda * 2 + mofs);
+          }
         }
         // B: hi and lo parts, NPAD rows x 8 chunks each
         unsigned char* sb = st + NMAT * kA;
@@ -290,46 +317,71 @@ __global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
   }
 }
 
+// The partial products are laid out [ks][rows][npad]: one row's npad values
+// are contiguous, so the finishers below give each thread four tokens of one
+// row (a 16-byte load per K split) and let consecutive threads take
+// consecutive rows, which keeps their 16-bit outputs [npad][rows] coalesced.
+
+// Sum over the K splits of tokens 4nq..4nq+3 of one row, in split order.
+__device__ __forceinline__ float4 sum_splits(const float* D, int ks, size_t split_stride, size_t off) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int kq = 0; kq < ks; ++kq) {
+    const float4 v = ld_dep4(D + (size_t)kq * split_stride + off);
+    a.x += v.x;
+    a.y += v.y;
+    a.z += v.z;
+    a.w += v.w;
+  }
+  return a;
+}
+
+__device__ __forceinline__ float f4_get(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
 // hid[n][j] = ReLU(sum_kq D[kq][j][n] + b1[j]) as hi/lo parts [2][npad][h].
+// Thread i = nq * h + j.
 template <typename T>
 __global__ void k_b_hidden_fin(const float* D, int ks, int mrows, int npad, int h, int B, const float* b1, T* out) {
   pdl_launch_dependents();
   pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = n * h + j
-  if (i >= npad * h) return;
-  const int n = i / h, j = i % h;
-  float v = 0.f;
-  if (n < B) {
-    float s = 0.f;
-    for (int kq = 0; kq < ks; ++kq) s += ld_dep(D + ((size_t)kq * mrows + j) * npad + n);
-    if (b1) s += b1[j];
-    v = relu_nan(s);
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (npad / 4) * h) return;
+  const int nq = i / h, j = i % h;
+  const float4 a = sum_splits(D, ks, (size_t)mrows * npad, (size_t)j * npad + nq * 4);
+  const float bias = b1 ? b1[j] : 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int n = nq * 4 + e;
+    const float v = n < B ? relu_nan(f4_get(a, e) + bias) : 0.f;
+    T hi, lo;
+    split16<T>(v, hi, lo);
+    out[(size_t)n * h + j] = hi;
+    out[(size_t)npad * h + (size_t)n * h + j] = lo;
   }
-  T hi, lo;
-  split16<T>(v, hi, lo);
-  out[i] = hi;
-  out[(size_t)npad * h + i] = lo;
 }
 
-// nmask[n][w] for every token n < B: one warp per mask word, one ballot per token.
+// nmask[n][w] for every token n < B: one warp per (mask word, token quad),
+// lane = row of the word, one ballot per token.
 __global__ void k_b_scores_fin(const float* D, int ks, int mrows, int npad, int nw, int B, const float* b2,
                                float thres, uint32_t* nmask) {
   pdl_launch_dependents();
   pdl_wait();
-  const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
-  if (w >= nw) return;
+  const int nq = gw / nw, w = gw % nw;
+  if (nq >= npad / 4 || nq * 4 >= B) return;
   const int row = w * 32 + lane;
+  const float4 a = sum_splits(D, ks, (size_t)mrows * npad, (size_t)row * npad + nq * 4);
   const float bias = b2 ? b2[row] : 0.f;
   uint32_t mine = 0;
-  for (int n = 0; n < B; ++n) {
-    float s = 0.f;
-    for (int kq = 0; kq < ks; ++kq) s += ld_dep(D + ((size_t)kq * mrows + row) * npad + n);
-    s += bias;
-    const uint32_t m = __ballot_sync(SFFN_FULL_MASK, s >= thres);  // NaN compares false
-    if (lane == n) mine = m;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t m = __ballot_sync(SFFN_FULL_MASK, f4_get(a, e) + bias >= thres);  // NaN compares false
+    if (lane == e) mine = m;
   }
-  if (lane < B) nmask[(size_t)lane * nw + w] = mine;
+  const int n = nq * 4 + lane;
+  if (lane < 4 && n < B) nmask[(size_t)n * nw + w] = mine;
 }
 
 // Views: block b < B expands token b's mask (index list, count, group mask);
@@ -370,53 +422,67 @@ __global__ void __launch_bounds__(kViewThreadsB)
   }
 }
 
-// H parts [2][npad][ldh]: h = act(g, u) for union neuron i and token n if the
+// H parts [2][npad][ldh]: h = act(g, u) for union neuron u and token n if the
 // neuron is in token n's own mask, else 0; zero beyond the union and for n >= B.
+// Thread i = nq * ldh + u.
 template <typename T, int ACT>
 __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32_t* ucount,
                             const int32_t* uidx, const uint32_t* nmask, int nw, int npad, int B, int ldh,
                             int target, T* H) {
   pdl_launch_dependents();
   pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (npad / 4) * ldh) return;
+  const int nq = i / ldh, u = i % ldh;
   const int U = ld_dep(ucount);
-  const Plan p = make_plan(false, U, d, target);  // the up/gate product's plan (K = d)
-  const size_t total = (size_t)npad * ldh;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int n = (int)(i / ldh), u = (int)(i % ldh);
-    float v = 0.f;
-    if (n < B && u < U) {
-      const int slot = ld_dep(uidx + u);
-      if ((ld_dep(nmask + (size_t)n * nw + (slot >> 5)) >> (slot & 31)) & 1u) {
-        const size_t mrows = (size_t)p.m_tiles * kTileM;
-        float uu = 0.f, gg = 0.f;
-        for (int kq = 0; kq < p.ks; ++kq) {
-          uu += ld_dep(Du + ((size_t)kq * mrows + u) * npad + n);
-          if (ACT != SFFN_ACT_RELU) gg += ld_dep(Dg + ((size_t)kq * mrows + u) * npad + n);
-        }
-        v = neuron_act<ACT>(uu, gg);
-      }
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (u < U && nq * 4 < B) {
+    const Plan p = make_plan(false, U, d, target);  // the up/gate product's plan (K = d)
+    const size_t sstride = (size_t)p.m_tiles * kTileM * npad;
+    const size_t off = (size_t)u * npad + nq * 4;
+    const float4 au = sum_splits(Du, p.ks, sstride, off);
+    const float4 ag = ACT != SFFN_ACT_RELU ? sum_splits(Dg, p.ks, sstride, off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int slot = ld_dep(uidx + u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = nq * 4 + e;
+      if (n < B && ((ld_dep(nmask + (size_t)n * nw + (slot >> 5)) >> (slot & 31)) & 1u))
+        v[e] = neuron_act<ACT>(f4_get(au, e), f4_get(ag, e));
     }
+  }
+  const size_t total = (size_t)npad * ldh;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const size_t o = (size_t)(nq * 4 + e) * ldh + u;
     T hi, lo;
-    split16<T>(v, hi, lo);
-    H[i] = hi;
-    H[total + i] = lo;
+    split16<T>(v[e], hi, lo);
+    H[o] = hi;
+    H[total + o] = lo;
   }
 }
 
-// y[n][c] = sum_kq D[kq][c][n]; x_out = x + y.
+// y[n][c] = sum_kq D[kq][c][n]; x_out = x + y. Thread i = nq * d + c.
 __global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad, int B, int target, const float* x,
                           float* y, float* x_out) {
   pdl_launch_dependents();
   pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (npad / 4) * d) return;
+  const int nq = i / d, c = i % d;
+  if (nq * 4 >= B) return;
   const int U = ld_dep(ucount);
   const Plan p = make_plan(true, U, d, target);
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // i = n * d + c
-  if (i >= B * d) return;
-  const int n = i / d, c = i % d;
-  float s = 0.f;
-  for (int kq = 0; kq < p.ks; ++kq) s += ld_dep(D + ((size_t)kq * d + c) * npad + n);
-  y[i] = s;
-  if (x_out) x_out[i] = ld_dep(x + i) + s;
+  const float4 a = sum_splits(D, p.ks, (size_t)d * npad, (size_t)c * npad + nq * 4);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int n = nq * 4 + e;
+    if (n < B) {
+      const size_t o = (size_t)n * d + c;
+      const float s = f4_get(a, e);
+      y[o] = s;
+      if (x_out) x_out[o] = ld_dep(x + o) + s;
+    }
+  }
 }
 
 }  // namespace
@@ -568,7 +634,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     if (e != cudaSuccess) return e;
     const Plan ph = make_plan(false, h, d, target);
     void* hidhl = base + w.hidhl;
-    const int hb = (npad * h + 255) / 256;
+    const int hb = ((npad / 4) * h + 255) / 256;
     const float* b1 = L.has_b1 ? L.b1 : nullptr;
     if (bf)
       e = launch_ex(k_b_hidden_fin<__nv_bfloat16>, dim3(hb), dim3(256), 0, st, true, 1,
@@ -593,7 +659,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     if (e != cudaSuccess) return e;
     const Plan ps = make_plan(false, f, h, target);
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
-    e = launch_ex(k_b_scores_fin, dim3((nw + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
+    e = launch_ex(k_b_scores_fin, dim3((nw * (npad / 4) + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
                   ps.ks, ps.m_tiles * kTileM, npad, nw, B, b2, thres, m->nmask);
     if (e != cudaSuccess) return e;
   }
@@ -626,7 +692,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   if (e != cudaSuccess) return e;
   // activation with each token's own mask -> H parts [2][npad][fpad]
   void* hhl = base + w.hhl;
-  const int ab = std::min(2048, (npad * fpad + 255) / 256);
+  const int ab = ((npad / 4) * fpad + 255) / 256;
 #define SFFN_ACT_LAUNCH(T, A)                                                                                     \
   launch_ex(k_b_act_fin<T, A>, dim3(ab), dim3(256), 0, st, true, 1, static_cast<const float*>(u.D),              \
             static_cast<const float*>(u.D + dmat), d, static_cast<const int32_t*>(ucount),                        \
@@ -653,7 +719,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.err = L.err;
   e = traced_b(L, 3, st, [&] { return launch_gemm_n<true, 1>(L, npad, dn, st); });
   if (e != cudaSuccess) return e;
-  return launch_ex(k_b_y_fin, dim3((B * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
+  return launch_ex(k_b_y_fin, dim3(((npad / 4) * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
                    static_cast<const int32_t*>(ucount), d, npad, B, target, x, y, x_out);
 }
 
