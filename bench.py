@@ -295,7 +295,11 @@ def run_ours(args, world, rank, local):
     tok_counts = np.zeros((P, nL), dtype=np.int64)   # sum over tokens of their own active neurons
     with torch.cuda.stream(stream):
         for t in range(P):
-            step(t)
+            xl = step(t)
+            if not bool(torch.isfinite(xl).all()):
+                raise SystemExit(f"{spec.name}: the residual stream overflowed within {nL} layers (a gated FFN grows "
+                                 "with the square of its input and this stack has no block normalisation); "
+                                 "use --layers to shorten it")
             if Bt == 1:
                 counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
                 tok_counts[t] = counts[t]
@@ -402,20 +406,54 @@ def run_ours(args, world, rank, local):
     tam_us = 1e3 * sum(a.elapsed_time(b) for a, b in tam_ev) / R
     dom = max(KN, key=lambda k: per_kernel[k]["us"])
 
-    # ---- dense run of the same layer: every neuron active (thres = -inf)
-    dense_us = None
+    # ---- dense run of the same layer: every FFN row, no predictor. (1) our
+    # kernels on an all-active caller mask (sffn_forward); (2) the library
+    # reference: the same FFN as cuBLAS GEMVs on the packed weights (torch
+    # matmul with 16-bit x, fp32 accumulation inside cuBLAS), for context.
+    nd = 20
+    dense_masks = [layers[l].masks(Bt, device=dev) for l in range(nL)]
+    for m in dense_masks:
+        m.nmask.fill_(-1)
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for i in range(3):
-            sffn.sffn_decode_step(layers[0].handle, X[i % P], Bt, float("-inf"), masks[0], ybuf, xa, ws, stream)
+            sffn.sffn_forward(layers[0].handle, X[i % P], Bt, dense_masks[0], ybuf, None, ws, stream)
         e0.record(stream)
-        nd = 20
         for i in range(nd):
-            sffn.sffn_decode_step(layers[i % nL].handle, X[i % P], Bt, float("-inf"), masks[i % nL], ybuf, xa, ws,
-                                  stream)
+            sffn.sffn_forward(layers[i % nL].handle, X[i % P], Bt, dense_masks[i % nL], ybuf, None, ws, stream)
         e1.record(stream)
     torch.cuda.synchronize()
     dense_us = 1e3 * e0.elapsed_time(e1) / nd
+    dense_lib_us = None
+    if spec.wdtype != "f32":
+        tdt = torch.bfloat16 if spec.wdtype == "bf16" else torch.float16
+        views = []
+        for L in layers:
+            pv = L.packed()
+            mk = lambda ptr: sffn.view_device(ptr, (spec.f, spec.d), tdt)
+            views.append((mk(pv.up), mk(pv.gate) if spec.act != "relu" else None, mk(pv.downT)))
+
+        def dense_lib(l, xv):
+            up, gate, downT = views[l]
+            xt = xv.to(tdt).t()                      # [d][B]
+            u = torch.matmul(up, xt)                 # [f][B]
+            if spec.act == "relu":
+                hh = torch.relu(u)
+            else:
+                g = torch.matmul(gate, xt)
+                hh = (torch.relu(g) if spec.act == "reglu" else torch.nn.functional.silu(g)) * u
+            return torch.matmul(hh.t(), downT)       # [B][d]
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                dense_lib(0, X[i % P])
+            e0.record(stream)
+            for i in range(nd):
+                dense_lib(i % nL, X[i % P])
+            e1.record(stream)
+        torch.cuda.synchronize()
+        dense_lib_us = 1e3 * e0.elapsed_time(e1) / nd
+        del views
 
     # ---- end to end through the public API with host buffers
     Xh = X.cpu().pin_memory()
@@ -481,6 +519,8 @@ def run_ours(args, world, rank, local):
         "algorithmic_hbm_frac": round(step_gbs / peak, 4),
         "dense_us_per_layer": round(dense_us, 3),
         "dense_speedup": round(dense_us / (1e3 * ms_per_step / nL), 3),
+        "dense_cublas_us_per_layer": round(dense_lib_us, 3) if dense_lib_us is not None else None,
+        "dense_note": "all FFN rows, no predictor: our kernels on an all-active mask; cuBLAS GEMVs as reference",
         "kernels_us": {k: round(v["us"], 3) for k, v in per_kernel.items()} | {"tam_all_layers": round(tam_us, 3)},
         "kernels_gbs": {k: round(v["gbs"], 1) for k, v in per_kernel.items()},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(pk["gbs"], 1), "peak": peak,
