@@ -230,6 +230,13 @@ sffn_status sffn_layer_set_trace(sffn_layer* L, const sffn_trace* t) {
   return SFFN_OK;
 }
 
+sffn_status sffn_layer_set_next(sffn_layer* L, const sffn_layer* next) {
+  if (!L) return invalid("layer is NULL");
+  if (next && next->device != L->device) return invalid("sffn_layer_set_next: next lives on another device");
+  L->next = next;
+  return SFFN_OK;
+}
+
 size_t sffn_workspace_bytes(const sffn_layer* L, int32_t B) {
   if (!L || B < 1 || B > L->desc.max_batch) return 0;
   return ws_bytes_for(*L, B);

@@ -36,12 +36,21 @@ constexpr int kReduceGroups = kReduceThreads / (kReduceCols / 4);  // 32 partial
 
 __device__ __forceinline__ void consumer_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
+// Block b's share (1/nb, 16-byte granules) of [base, base + bytes), handed to
+// L2 as bulk prefetches of at most 64 KB.
+__device__ __forceinline__ void prefetch_share(const unsigned char* base, size_t bytes, int b, int nb) {
+  if (!base) return;
+  const size_t units = bytes / 16;
+  const size_t lo = units * (size_t)b / (size_t)nb * 16, hi = units * (size_t)(b + 1) / (size_t)nb * 16;
+  for (size_t o = lo; o < hi; o += 65536) prefetch_l2_bulk(base + o, (uint32_t)min(hi - o, (size_t)65536));
+}
+
 template <typename T, int ACT, int CPT>
 __global__ void __launch_bounds__(kFfnThreads, 1)
     k_ffn(const T* __restrict__ up, const T* __restrict__ gate, const T* __restrict__ downT, const float* x,
           const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages, int list_cap,
           int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, uint32_t* __restrict__ gmask_out,
-          float* __restrict__ partials, uint32_t* __restrict__ err) {
+          float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes) {
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = ACT != SFFN_ACT_RELU;
@@ -116,6 +125,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
             bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s], pol);
         }
       }
+      // L2 hint: once this block's rows are all requested, its share of the
+      // next layer's predictor hidden-layer weights (pf is null without a hint)
+      if (!*(volatile int*)&s_abort) prefetch_share(pf, pf_bytes, b, nb);
     }
   } else {
     // ---------------- consumers, phase A: partial dot products of up/gate rows
@@ -280,9 +292,15 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
   const T* up = static_cast<const T*>(L.up);
   const T* gate = static_cast<const T*>(L.gate);
   const T* downT = static_cast<const T*>(L.downT);
+  // The optional L2 hint: the next layer's W1 only. Its 16.8 MB (70B shape)
+  // fit the HBM time that this kernel's tail and the reduction leave idle;
+  // adding W2 as well competed with this kernel's own row stream and lost.
+  const sffn_layer* nx = L.next;
+  const unsigned char* pf = nx ? static_cast<const unsigned char*>(nx->W1) : nullptr;
+  const size_t pf_bytes = nx ? (size_t)nx->desc.h * nx->desc.d * nx->wbytes : 0;
 #define SFFN_FFN_ARGS                                                                                         \
   grid, dim3(kFfnThreads), smem, st, true, 1, up, gate, downT, x, nmask, L.nwords, L.n_groups,                \
-      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err
+      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes
   switch (cpt) {
     case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
     case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);

@@ -31,6 +31,9 @@ struct sffn_layer {
   // launch shapes chosen at create time
   int score_stages = 0;     // predictor-scores ring depth (one mask word per stage)
   int ffn_stages = 0;       // fused FFN ring depth (one neuron's up/gate rows, or as many downT rows)
+  // optional L2 hint (sffn_layer_set_next): the layer whose predictor weights
+  // this layer's FFN kernel prefetches
+  const sffn_layer* next = nullptr;
   // optional timing hooks (sffn_layer_set_trace)
   cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};

@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=300)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefetch-next", action="store_true",
+                   help="do not let each layer prefetch the next layer's predictor weights into L2")
     p.add_argument("--ref-max-steps", type=int, default=24)
     return p.parse_args()
 
@@ -237,6 +239,12 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     with_b2 = spec.bias_mode
+    # L2 hint: each layer's FFN kernel warms the next layer's predictor weights
+    # (the last layer warms layer 0 for the next token)
+    prefetch_next = Bt == 1 and not args.no_prefetch_next
+    if prefetch_next:
+        for l in range(nL):
+            layers[l].set_next(layers[(l + 1) % nL])
 
     # ---- buffers
     P = max(1, min(args.tokens, spec.tokens))
@@ -509,7 +517,7 @@ def run_ours(args, world, rank, local):
             "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": nL, "batch": Bt,
             "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype, "thres": spec.thres,
             "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
-            "distinct_tokens": P, "graphs": graphs is not None,
+            "distinct_tokens": P, "graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
             "l2": "inputs larger than L2: each step reads %.2f GB of distinct weights" % (timed_bytes / args.steps / 1e9),
             "parallelism": "replicas" if world > 1 else "single",
         },

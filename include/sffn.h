@@ -179,6 +179,20 @@ typedef struct {
 
 sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* host, or NULL */);
 
+/* Optional L2 hint for a layer stack at B = 1. `next` names the layer whose
+ * hot call follows this layer's on the same stream (in a stack: layer l + 1,
+ * and for the last layer layer 0 of the next token), or NULL to turn the hint
+ * off. Each block of this layer's sparse-FFN kernel then asks L2 to fetch its
+ * share of next's predictor hidden-layer weights (W1, PowerInfer §5.1) once
+ * it has issued the copies of its own rows, so that those bytes move while
+ * other blocks finish and while the reduction runs; the next predictor then
+ * reads them from L2. Results are unchanged (the
+ * prefetch only warms the cache). The library does not own `next`: the caller
+ * keeps it alive while the hint is set, or unsets it first. `next` must live
+ * on the same device; it may equal `layer`. Host only.
+ * Errors: INVALID_ARG (layer NULL, or next on another device). */
+sffn_status sffn_layer_set_next(sffn_layer* layer, const sffn_layer* next /* or NULL */);
+
 /* ---------------------------------------------------------------- hot calls */
 
 /* Predictor (PowerInfer §5.1 and the threshold note): for each token b,

@@ -188,6 +188,28 @@ def test_deterministic(sffn):
     assert torch.equal(y1, y2)
 
 
+def test_l2_hint_leaves_results_unchanged(sffn):
+    """sffn_layer_set_next only warms L2: masks, y and x + y are bit-identical
+    with the hint on (to another layer, to the layer itself) and off."""
+    spec = W.spec_replace(W.WORKLOADS["llama2_70b_reglu_d8192_f28672_bf16_8l"], f=4096, tam_capacity=None)
+    A, _, _ = make_layer(spec, seed=0, layer=0)
+    Bl, _, _ = make_layer(spec, seed=0, layer=1)
+    x = W.make_tokens(spec.d, 1, seed=2, kind="ar1", device="cuda")[0]
+    m0, y0, xo0 = _decode(sffn, A, x, 0.0, x_out=True)
+    for nxt in (Bl, A, None):
+        A.set_next(nxt)
+        m1, y1, xo1 = _decode(sffn, A, x, 0.0, x_out=True)
+        assert torch.equal(y0, y1) and torch.equal(xo0, xo1)
+        for k in ("nmask", "gmask", "idx", "count"):
+            assert torch.equal(getattr(m0, k), getattr(m1, k)), k
+    A.set_next(Bl)
+    y2 = torch.empty(1, spec.d, device="cuda")
+    m2 = A.masks()
+    sffn.sffn_decode_step_static_ws(A.handle, x, 1, 0.0, m2, y2, None)
+    assert torch.equal(y0, y2)
+    A.check_error()
+
+
 # ------------------------------------------------------------------ tiny workload: 64 tokens with momentum
 
 def test_tiny_sequence_with_tam(sffn):
