@@ -43,18 +43,26 @@ struct GemmArgs {
   int lda;                  // elements per A row
   const unsigned char* Bhl; // [2][npad][ldb] 16-bit hi then lo parts, K-major
   int ldb;
-  float* D;                 // partials [ks][m_tiles * 128][npad]
+  float* D;                 // partial tiles [slot][128][npad] (slot = CTA + tile, see Plan)
   size_t dmat_stride;       // floats from the first matrix's partials to the second's
-  int target_units;
+  int grid;                 // CTAs launched
   uint32_t* err;
 };
 
-// Work decomposition shared by the GEMM and its finishers.
+// Work decomposition shared by the GEMM and its finishers (stream-K): the
+// m_tiles x kblocks (tile, K block) pairs, tile after tile, are cut into
+// `ctas` equal contiguous ranges, one per CTA, so every CTA streams the same
+// number of K blocks. A CTA writes one partial tile for every tile its range
+// touches, at slot CTA + tile (unique: a later CTA starts where the earlier
+// one ends); the CTAs touching tile t are cta_of(t * kblocks) ..
+// cta_of((t + 1) * kblocks - 1), whose partials the finishers add in CTA
+// order.
 struct Plan {
-  int m_tiles, kblocks, ks, units;
+  int m_tiles, kblocks, ctas;
+  long long total;
 };
 
-__host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, int target) {
+__host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, int grid) {
   Plan p;
   if (!mn_major) {
     p.m_tiles = (count + kTileM - 1) / kTileM;
@@ -63,16 +71,17 @@ __host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, i
     p.m_tiles = other / kTileM;
     p.kblocks = (count + kTileK - 1) / kTileK;
   }
-  if (p.m_tiles == 0 || p.kblocks == 0) {
-    p.ks = 0;
-    p.units = 0;
-    return p;
-  }
-  int ks = (target + p.m_tiles - 1) / p.m_tiles;
-  ks = ks < 1 ? 1 : (ks > p.kblocks ? p.kblocks : ks);
-  p.ks = ks;
-  p.units = p.m_tiles * ks;
+  p.total = (long long)p.m_tiles * p.kblocks;
+  p.ctas = (int)(p.total < grid ? p.total : grid);
   return p;
+}
+
+// First linear (tile, K block) index of CTA b's range.
+__host__ __device__ inline long long range_lo(const Plan& p, int b) { return p.total * b / p.ctas; }
+
+// The CTA whose range holds linear index x (p.total > 0).
+__host__ __device__ inline int cta_of(const Plan& p, long long x) {
+  return (int)(((x + 1) * p.ctas - 1) / p.total);
 }
 
 template <bool MN, int NMAT, int NPAD>
@@ -113,12 +122,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
   pdl_launch_dependents();
   pdl_wait();  // operands and row lists come from earlier kernels
   const int count = g.count_dev ? ld_dep(g.count_dev) : g.fixed_count;
-  const Plan p = make_plan(MN, count, g.other, g.target_units);
-  const size_t mrows = (size_t)p.m_tiles * kTileM;
-
-  auto krange = [&](int kq, int& kb0, int& kb1) {
-    kb0 = (int)((long long)p.kblocks * kq / p.ks);
-    kb1 = (int)((long long)p.kblocks * (kq + 1) / p.ks);
+  const Plan p = make_plan(MN, count, g.other, g.grid);
+  const int cta = blockIdx.x;
+  const long long r_lo = cta < p.ctas ? range_lo(p, cta) : 0;
+  const long long r_hi = cta < p.ctas ? range_lo(p, cta + 1) : 0;
+  // segment [i0, i1) of this CTA's range inside tile mt, K blocks [kb0, kb1)
+  auto segment = [&](long long i0, int& mt, int& kb0, int& kb1, long long& i1) {
+    mt = (int)(i0 / p.kblocks);
+    const long long tile_end = (long long)(mt + 1) * p.kblocks;
+    i1 = r_hi < tile_end ? r_hi : tile_end;
+    kb0 = (int)(i0 - (long long)mt * p.kblocks);
+    kb1 = (int)(i1 - (long long)mt * p.kblocks);
   };
 
   if (warp < 4) {
@@ -130,10 +144,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
     const int j8 = tid & 7, r8 = tid >> 3;
     const int c16 = tid & 15, k16 = tid >> 4;
     int it = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-      const int mt = u / p.ks, kq = u % p.ks;
-      int kb0, kb1;
-      krange(kq, kb0, kb1);
+    for (long long i0 = r_lo, i1 = 0; i0 < r_hi; i0 = i1) {
+      int mt, kb0, kb1;
+      segment(i0, mt, kb0, kb1, i1);
       // K-major: byte offsets of this thread's eight rows, fixed over the unit.
       size_t roff[8];
       // MN-major: the warp's gathered rows for eight stages, four per lane:
@@ -205,10 +218,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
     const int ew = warp - 4;  // TMEM lane quarter of this warp
     int it = 0, ui = 0;
     bool issued = false;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++ui) {
-      const int mt = u / p.ks, kq = u % p.ks;
-      int kb0, kb1;
-      krange(kq, kb0, kb1);
+    for (long long i0 = r_lo, i1 = 0; i0 < r_hi; i0 = i1, ++ui) {
+      int mt, kb0, kb1;
+      segment(i0, mt, kb0, kb1, i1);
       if (warp == 4 && lane == 0) {
         bool ok = ui == 0 || mbar_wait_bounded(dempty, (uint32_t)((ui - 1) & 1));
         if (ok) tc::fence_after();
@@ -254,10 +266,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
         break;
       }
       tc::fence_after();
-      const size_t row = (size_t)mt * kTileM + ew * 32 + lane;
+      const size_t row = (size_t)(cta + mt) * kTileM + ew * 32 + lane;  // slot cta + mt
 #pragma unroll
       for (int a = 0; a < NMAT; ++a) {
-        float* dst = g.D + (size_t)a * g.dmat_stride + ((size_t)kq * mrows + row) * NPAD;
+        float* dst = g.D + (size_t)a * g.dmat_stride + row * NPAD;
 #pragma unroll
         for (int c0 = 0; c0 < NPAD; c0 += 16) {
           float v[16];
@@ -317,16 +329,20 @@ __global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
   }
 }
 
-// The partial products are laid out [ks][rows][npad]: one row's npad values
+// The partial tiles are laid out [slot][128][npad]: one row's npad values
 // are contiguous, so the finishers below give each thread four tokens of one
-// row (a 16-byte load per K split) and let consecutive threads take
+// row (a 16-byte load per partial) and let consecutive threads take
 // consecutive rows, which keeps their 16-bit outputs [npad][rows] coalesced.
 
-// Sum over the K splits of tokens 4nq..4nq+3 of one row, in split order.
-__device__ __forceinline__ float4 sum_splits(const float* D, int ks, size_t split_stride, size_t off) {
+// Tokens 4nq..4nq+3 of output row `row`: the partials of the CTAs that touched
+// its tile, added in CTA order (zero when the product is empty).
+__device__ __forceinline__ float4 sum_segments(const float* D, const Plan& p, int row, int npad, int nq) {
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int kq = 0; kq < ks; ++kq) {
-    const float4 v = ld_dep4(D + (size_t)kq * split_stride + off);
+  if (p.total == 0) return a;
+  const int mt = row / kTileM, rr = row % kTileM;
+  const int b0 = cta_of(p, (long long)mt * p.kblocks), b1 = cta_of(p, (long long)(mt + 1) * p.kblocks - 1);
+  for (int b = b0; b <= b1; ++b) {
+    const float4 v = ld_dep4(D + ((size_t)(b + mt) * kTileM + rr) * npad + nq * 4);
     a.x += v.x;
     a.y += v.y;
     a.z += v.z;
@@ -342,13 +358,14 @@ __device__ __forceinline__ float f4_get(const float4& v, int i) {
 // hid[n][j] = ReLU(sum_kq D[kq][j][n] + b1[j]) as hi/lo parts [2][npad][h].
 // Thread i = nq * h + j.
 template <typename T>
-__global__ void k_b_hidden_fin(const float* D, int ks, int mrows, int npad, int h, int B, const float* b1, T* out) {
+__global__ void k_b_hidden_fin(const float* D, int d, int grid, int npad, int h, int B, const float* b1, T* out) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (npad / 4) * h) return;
   const int nq = i / h, j = i % h;
-  const float4 a = sum_splits(D, ks, (size_t)mrows * npad, (size_t)j * npad + nq * 4);
+  const Plan p = make_plan(false, h, d, grid);  // the hidden product's plan (K = d)
+  const float4 a = sum_segments(D, p, j, npad, nq);
   const float bias = b1 ? b1[j] : 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -363,7 +380,7 @@ __global__ void k_b_hidden_fin(const float* D, int ks, int mrows, int npad, int 
 
 // nmask[n][w] for every token n < B: one warp per (mask word, token quad),
 // lane = row of the word, one ballot per token.
-__global__ void k_b_scores_fin(const float* D, int ks, int mrows, int npad, int nw, int B, const float* b2,
+__global__ void k_b_scores_fin(const float* D, int h, int grid, int npad, int nw, int B, const float* b2,
                                float thres, uint32_t* nmask) {
   pdl_launch_dependents();
   pdl_wait();
@@ -372,7 +389,8 @@ __global__ void k_b_scores_fin(const float* D, int ks, int mrows, int npad, int 
   const int nq = gw / nw, w = gw % nw;
   if (nq >= npad / 4 || nq * 4 >= B) return;
   const int row = w * 32 + lane;
-  const float4 a = sum_splits(D, ks, (size_t)mrows * npad, (size_t)row * npad + nq * 4);
+  const Plan p = make_plan(false, nw * 32, h, grid);  // the scores product's plan (K = h)
+  const float4 a = sum_segments(D, p, row, npad, nq);
   const float bias = b2 ? b2[row] : 0.f;
   uint32_t mine = 0;
 #pragma unroll
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(kViewThreadsB)
 template <typename T, int ACT>
 __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32_t* ucount,
                             const int32_t* uidx, const uint32_t* nmask, int nw, int npad, int B, int ldh,
-                            int target, T* H) {
+                            int grid, T* H) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -437,11 +455,9 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
   const int U = ld_dep(ucount);
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (u < U && nq * 4 < B) {
-    const Plan p = make_plan(false, U, d, target);  // the up/gate product's plan (K = d)
-    const size_t sstride = (size_t)p.m_tiles * kTileM * npad;
-    const size_t off = (size_t)u * npad + nq * 4;
-    const float4 au = sum_splits(Du, p.ks, sstride, off);
-    const float4 ag = ACT != SFFN_ACT_RELU ? sum_splits(Dg, p.ks, sstride, off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const Plan p = make_plan(false, U, d, grid);  // the up/gate product's plan (K = d)
+    const float4 au = sum_segments(Du, p, u, npad, nq);
+    const float4 ag = ACT != SFFN_ACT_RELU ? sum_segments(Dg, p, u, npad, nq) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int slot = ld_dep(uidx + u);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -462,7 +478,7 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
 }
 
 // y[n][c] = sum_kq D[kq][c][n]; x_out = x + y. Thread i = nq * d + c.
-__global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad, int B, int target, const float* x,
+__global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad, int B, int grid, const float* x,
                           float* y, float* x_out) {
   pdl_launch_dependents();
   pdl_wait();
@@ -471,8 +487,8 @@ __global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad
   const int nq = i / d, c = i % d;
   if (nq * 4 >= B) return;
   const int U = ld_dep(ucount);
-  const Plan p = make_plan(true, U, d, target);
-  const float4 a = sum_splits(D, p.ks, (size_t)d * npad, (size_t)c * npad + nq * 4);
+  const Plan p = make_plan(true, U, d, grid);
+  const float4 a = sum_segments(D, p, c, npad, nq);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int n = nq * 4 + e;
@@ -492,10 +508,10 @@ __global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad
 namespace {
 
 int npad_of(int B) { return B <= 16 ? 16 : 32; }
-int gemm_target(const sffn_layer& L) { return 2 * L.num_sms; }
+int gemm_grid(const sffn_layer& L) { return L.num_sms; }
 
 size_t rows_bound(const sffn_layer& L, int m_tiles_max) {
-  return ((size_t)gemm_target(L) + (size_t)m_tiles_max) * kTileM;
+  return ((size_t)gemm_grid(L) + (size_t)m_tiles_max) * kTileM;  // partial slots < CTAs + tiles
 }
 
 template <bool MN, int NMAT, int NPAD>
@@ -524,7 +540,7 @@ template <bool MN, int NMAT, int NPAD>
 cudaError_t launch_gemm(const sffn_layer& L, const GemmArgs& g, cudaStream_t st) {
   const int stages = gemm_stages<MN, NMAT, NPAD>();
   const size_t smem = gemm_smem<MN, NMAT, NPAD>(stages);
-  return launch_ex(k_tc_gemm<MN, NMAT, NPAD>, dim3(L.num_sms), dim3(kGemmThreads), smem, st, true, 1, g,
+  return launch_ex(k_tc_gemm<MN, NMAT, NPAD>, dim3(g.grid), dim3(kGemmThreads), smem, st, true, 1, g,
                    L.desc.wdtype == SFFN_BF16, stages);
 }
 
@@ -602,7 +618,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   const int d = L.desc.d, f = L.desc.f, h = L.desc.h, nw = L.nwords;
   const int fpad = (f + kTileK - 1) / kTileK * kTileK;
   const bool bf = L.desc.wdtype == SFFN_BF16;
-  const int target = gemm_target(L);
+  const int grid = gemm_grid(L);
   uint32_t* unmask = m->unmask ? m->unmask : reinterpret_cast<uint32_t*>(base + w.unmask);
   int32_t* uidx = m->uidx ? m->uidx : reinterpret_cast<int32_t*>(base + w.uidx);
   int32_t* ucount = m->ucount ? m->ucount : reinterpret_cast<int32_t*>(base + w.ucount);
@@ -628,21 +644,20 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     g.Bhl = static_cast<const unsigned char*>(xhl);
     g.ldb = d;
     g.D = reinterpret_cast<float*>(base + w.dh);
-    g.target_units = target;
+    g.grid = grid;
     g.err = L.err;
     e = traced_b(L, 0, st, [&] { return launch_gemm_n<false, 1>(L, npad, g, st); });
     if (e != cudaSuccess) return e;
-    const Plan ph = make_plan(false, h, d, target);
     void* hidhl = base + w.hidhl;
     const int hb = ((npad / 4) * h + 255) / 256;
     const float* b1 = L.has_b1 ? L.b1 : nullptr;
     if (bf)
       e = launch_ex(k_b_hidden_fin<__nv_bfloat16>, dim3(hb), dim3(256), 0, st, true, 1,
-                    static_cast<const float*>(g.D), ph.ks, ph.m_tiles * kTileM, npad, h, B, b1,
+                    static_cast<const float*>(g.D), d, grid, npad, h, B, b1,
                     static_cast<__nv_bfloat16*>(hidhl));
     else
       e = launch_ex(k_b_hidden_fin<__half>, dim3(hb), dim3(256), 0, st, true, 1, static_cast<const float*>(g.D),
-                    ph.ks, ph.m_tiles * kTileM, npad, h, B, b1, static_cast<__half*>(hidhl));
+                    d, grid, npad, h, B, b1, static_cast<__half*>(hidhl));
     if (e != cudaSuccess) return e;
     // scores: D[f x N] = W2 . HID^T over K = h
     GemmArgs s{};
@@ -653,14 +668,13 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     s.Bhl = static_cast<const unsigned char*>(hidhl);
     s.ldb = h;
     s.D = reinterpret_cast<float*>(base + w.ds);
-    s.target_units = target;
+    s.grid = grid;
     s.err = L.err;
     e = traced_b(L, 1, st, [&] { return launch_gemm_n<false, 1>(L, npad, s, st); });
     if (e != cudaSuccess) return e;
-    const Plan ps = make_plan(false, f, h, target);
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
     e = launch_ex(k_b_scores_fin, dim3((nw * (npad / 4) + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
-                  ps.ks, ps.m_tiles * kTileM, npad, nw, B, b2, thres, m->nmask);
+                  h, grid, npad, nw, B, b2, thres, m->nmask);
     if (e != cudaSuccess) return e;
   }
   // per-token views (when predicting) and the union mask with its views
@@ -684,7 +698,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   u.ldb = d;
   u.D = reinterpret_cast<float*>(base + w.dug);
   u.dmat_stride = dmat;
-  u.target_units = target;
+  u.grid = grid;
   u.err = L.err;
   e = traced_b(L, 2, st, [&] {
     return gated ? launch_gemm_n<false, 2>(L, npad, u, st) : launch_gemm_n<false, 1>(L, npad, u, st);
@@ -696,7 +710,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
 #define SFFN_ACT_LAUNCH(T, A)                                                                                     \
   launch_ex(k_b_act_fin<T, A>, dim3(ab), dim3(256), 0, st, true, 1, static_cast<const float*>(u.D),              \
             static_cast<const float*>(u.D + dmat), d, static_cast<const int32_t*>(ucount),                        \
-            static_cast<const int32_t*>(uidx), static_cast<const uint32_t*>(m->nmask), nw, npad, B, fpad, target, \
+            static_cast<const int32_t*>(uidx), static_cast<const uint32_t*>(m->nmask), nw, npad, B, fpad, grid, \
             static_cast<T*>(hhl))
   switch (L.desc.act) {
     case SFFN_ACT_RELU: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_RELU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_RELU); break;
@@ -715,12 +729,12 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.Bhl = static_cast<const unsigned char*>(hhl);
   dn.ldb = fpad;
   dn.D = reinterpret_cast<float*>(base + w.dy);
-  dn.target_units = target;
+  dn.grid = grid;
   dn.err = L.err;
   e = traced_b(L, 3, st, [&] { return launch_gemm_n<true, 1>(L, npad, dn, st); });
   if (e != cudaSuccess) return e;
   return launch_ex(k_b_y_fin, dim3(((npad / 4) * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
-                   static_cast<const int32_t*>(ucount), d, npad, B, target, x, y, x_out);
+                   static_cast<const int32_t*>(ucount), d, npad, B, grid, x, y, x_out);
 }
 
 }  // namespace sffn
