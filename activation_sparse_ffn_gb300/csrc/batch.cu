@@ -19,7 +19,11 @@
 #include "scan.cuh"
 #include "tcgen05.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 #include <string>
 
 namespace sffn {
@@ -30,10 +34,12 @@ constexpr int kGemmThreads = 256;    // warps 0-3 producers, warp 4 MMA issuer, 
 constexpr int kProducers = 128;
 constexpr int kTileM = 128;
 constexpr int kTileK = 64;
-constexpr int kGemmSmemBudget = 200 * 1024;
+constexpr int kGemmSmemBudget = 221 * 1024;
 constexpr int kViewThreadsB = 1024;
 
 struct GemmArgs {
+  CUtensorMap tmA;          // contiguous A rows (products without a row list): box 64 K x 128 rows
+  CUtensorMap tmB;          // B parts [2 * npad][ldb]: box 64 K x npad rows
   const unsigned char* A0;  // first A matrix
   const unsigned char* A1;  // second A matrix with the same rows (gate), or null
   const int32_t* rows;      // gathered rows of A (null: row i is row i)
@@ -50,25 +56,29 @@ struct GemmArgs {
 };
 
 // Work decomposition shared by the GEMM and its finishers (stream-K): the
-// m_tiles x kblocks (tile, K block) pairs, tile after tile, are cut into
+// m_tiles x kblocks (tile, K step) pairs, tile after tile, are cut into
 // `ctas` equal contiguous ranges, one per CTA, so every CTA streams the same
-// number of K blocks. A CTA writes one partial tile for every tile its range
-// touches, at slot CTA + tile (unique: a later CTA starts where the earlier
-// one ends); the CTAs touching tile t are cta_of(t * kblocks) ..
+// number of ring stages. A CTA writes one partial tile for every tile its
+// range touches, at slot CTA + tile (unique: a later CTA starts where the
+// earlier one ends); the CTAs touching tile t are cta_of(t * kblocks) ..
 // cta_of((t + 1) * kblocks - 1), whose partials the finishers add in CTA
-// order.
+// order. A K step is `ksub` blocks of 64 (K-major products); an MN-major tile
+// is `msub` blocks of 128 output rows.
 struct Plan {
-  int m_tiles, kblocks, ctas;
+  int m_tiles, kblocks, ctas, tile_rows;
   long long total;
 };
 
-__host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, int grid) {
+__host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, int grid, int ksub = 1,
+                                          int msub = 1) {
   Plan p;
   if (!mn_major) {
+    p.tile_rows = kTileM;
     p.m_tiles = (count + kTileM - 1) / kTileM;
-    p.kblocks = other / kTileK;
+    p.kblocks = other / (kTileK * ksub);
   } else {
-    p.m_tiles = other / kTileM;
+    p.tile_rows = kTileM * msub;
+    p.m_tiles = other / p.tile_rows;
     p.kblocks = (count + kTileK - 1) / kTileK;
   }
   p.total = (long long)p.m_tiles * p.kblocks;
@@ -76,7 +86,24 @@ __host__ __device__ inline Plan make_plan(bool mn_major, int count, int other, i
   return p;
 }
 
-// First linear (tile, K block) index of CTA b's range.
+// Ring-stage shapes. Each stage reads longer contiguous runs of every weight
+// row than one 128-byte K block: HBM serves such runs much faster than
+// scattered 128-byte pieces.
+//   contiguous rows (TMA): 4 K blocks (512 bytes per row) when K allows;
+__host__ __device__ inline int ksub_contig(int k) { return k % (4 * kTileK) == 0 ? 4 : 1; }
+//   gathered K-major rows (cp.async): 4 K blocks, 2 for up + gate (two stages fit);
+__host__ __device__ inline int ksub_gather(int k, int nmat) {
+  const int want = nmat == 2 ? 2 : 4;
+  if (k % (want * kTileK) == 0) return want;
+  return k % (2 * kTileK) == 0 ? 2 : 1;
+}
+//   gathered MN-major rows (down): 4 output tiles of 128 (1 KB per row) when d allows.
+__host__ __device__ inline int msub_down(int d) {
+  const int t = d / kTileM;
+  return t % 4 == 0 ? 4 : (t % 2 == 0 ? 2 : 1);
+}
+
+// First linear (tile, K step) index of CTA b's range.
 __host__ __device__ inline long long range_lo(const Plan& p, int b) { return p.total * b / p.ctas; }
 
 // The CTA whose range holds linear index x (p.total > 0).
@@ -84,17 +111,41 @@ __host__ __device__ inline int cta_of(const Plan& p, long long x) {
   return (int)(((x + 1) * p.ctas - 1) / p.total);
 }
 
-template <bool MN, int NMAT, int NPAD>
-__global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf16, int stages) {
-  constexpr uint32_t kA = kTileM * kTileK * 2;   // 16 KB per A tile
-  constexpr uint32_t kB = NPAD * kTileK * 2;     // one B part (hi or lo)
-  constexpr uint32_t kStage = NMAT * kA + 2 * kB;
-  constexpr uint32_t kCols = (NMAT * NPAD) <= 32 ? 32u : ((NMAT * NPAD) <= 64 ? 64u : 128u);
+// One persistent kernel per product. A tiles come from the TMA engine when the
+// rows are contiguous (GATHER false: the hidden and scores products) or from
+// coalesced cp.async copies of the gathered union rows (GATHER true); the B
+// tile of each K block (the activations' hi parts in rows 0..NPAD-1 and lo
+// parts in rows NPAD..2*NPAD-1) always comes from the TMA engine, so one MMA
+// of N = 2 * NPAD covers both parts and the epilogue adds the two halves.
+// Per ring stage, `tfull` counts the TMA bytes and `full` the 128 producer
+// threads' cp.async arrivals (GATHER only); the MMA thread waits for both.
+// Stage layout (every tile 1024-byte aligned): A tiles, then KSUB B tiles.
+//   K-major: A tiles [KSUB][NMAT] of 128 rows x 64 K.
+//   MN-major: A tiles [MSUB] of 128 M x 64 K (KSUB = 1, NMAT = 1).
+template <bool MN, int NMAT, int NPAD, bool GATHER, int KSUB, int MSUB>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_tc_gemm(const __grid_constant__ GemmArgs g, bool bf16, int stages) {
+  static_assert(!MN || (GATHER && KSUB == 1 && NMAT == 1), "the MN-major product gathers one K block per stage");
+  static_assert(MN || MSUB == 1, "output sub-tiles belong to the MN-major product");
+  static_assert(GATHER || NMAT == 1, "contiguous products have one A matrix");
+  constexpr int N2 = 2 * NPAD;                    // MMA N: hi rows then lo rows of B
+  constexpr uint32_t kA = kTileM * kTileK * 2;    // 16 KB per A tile
+  constexpr uint32_t kBt = N2 * kTileK * 2;       // B tile of one K block
+  constexpr int NACC = MN ? MSUB : NMAT;          // accumulators in tensor memory
+  constexpr uint32_t kATiles = MN ? MSUB : KSUB * NMAT;
+  constexpr uint32_t kStage = kATiles * kA + KSUB * kBt;
+  constexpr uint32_t kCols = NACC * N2 <= 32 ? 32u : (NACC * N2 <= 64 ? 64u : (NACC * N2 <= 128 ? 128u : 256u));
+  // gathered K-major rows: TPR threads per row cover its KSUB * 128 bytes
+  constexpr int TPR = KSUB * 8, RPI = kProducers / TPR, NIK = kTileM / RPI;
+  // gathered MN-major rows: TPK threads per K row cover its MSUB * 256 bytes
+  constexpr int TPK = MSUB * 16, RPK = kProducers / TPK, NIM = kTileK / RPK;
+  static_assert(!MN || NIM <= (TPK >= 32 ? 32 : 16), "row indices of a stage must fit one lane each");
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)stages * kStage);
-  uint64_t* empty = full + stages;
+  uint64_t* tfull = full + stages;
+  uint64_t* empty = tfull + stages;
   uint64_t* dfull = empty + stages;
   uint64_t* dempty = dfull + 1;
   uint64_t* drain = dempty + 1;
@@ -105,6 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], kProducers);
+      mbar_init(&tfull[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(dfull, 1);
@@ -122,11 +174,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
   pdl_launch_dependents();
   pdl_wait();  // operands and row lists come from earlier kernels
   const int count = g.count_dev ? ld_dep(g.count_dev) : g.fixed_count;
-  const Plan p = make_plan(MN, count, g.other, g.grid);
+  const Plan p = make_plan(MN, count, g.other, g.grid, KSUB, MSUB);
   const int cta = blockIdx.x;
   const long long r_lo = cta < p.ctas ? range_lo(p, cta) : 0;
   const long long r_hi = cta < p.ctas ? range_lo(p, cta + 1) : 0;
-  // segment [i0, i1) of this CTA's range inside tile mt, K blocks [kb0, kb1)
+  // segment [i0, i1) of this CTA's range inside tile mt, K steps [kb0, kb1)
   auto segment = [&](long long i0, int& mt, int& kb0, int& kb1, long long& i1) {
     mt = (int)(i0 / p.kblocks);
     const long long tile_end = (long long)(mt + 1) * p.kblocks;
@@ -135,44 +187,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
     kb1 = (int)(i1 - (long long)mt * p.kblocks);
   };
 
-  if (warp < 4) {
+  if (warp < 4 && (GATHER || tid == 0)) {
     // ------------------------------------------------------------ producers
-    // Each warp-wide copy instruction covers whole 128-byte lines. K-major:
-    // eight threads per row, thread t copies 16-byte chunk t & 7 of tile rows
-    // (t >> 3) + 16i. MN-major: sixteen threads per K row, thread t copies
-    // chunk t & 15 of the tile's 256 bytes of M in K rows (t >> 4) + 8i.
-    const int j8 = tid & 7, r8 = tid >> 3;
-    const int c16 = tid & 15, k16 = tid >> 4;
+    // K-major gathered rows: thread t copies 16-byte chunk t % TPR of rows
+    // t / TPR + RPI * i, so a warp instruction reads whole 128-byte lines.
+    // MN-major: thread t copies chunk t % TPK of K rows t / TPK + RPK * i;
+    // the rows of the next stage are held one per lane (lane l: K row
+    // k0 + RPK * l, k0 = t / TPK; with 16 threads per K row each half-warp
+    // holds its own) and handed out by shuffles. Thread 0 issues the TMA loads.
+    const uint64_t pol_a = l2_policy_evict_first();     // weights: read once per step
+    const uint64_t pol_b = tc::l2_policy_evict_last();  // activations: read by every CTA
+    const int k0 = tid / TPK;
+    const int hbase = TPK >= 32 ? 0 : (lane & 16), li = TPK >= 32 ? lane : (lane & 15);
     int it = 0;
     for (long long i0 = r_lo, i1 = 0; i0 < r_hi; i0 = i1) {
       int mt, kb0, kb1;
       segment(i0, mt, kb0, kb1, i1);
-      // K-major: byte offsets of this thread's eight rows, fixed over the unit.
-      size_t roff[8];
-      // MN-major: the warp's gathered rows for eight stages, four per lane:
-      // lane l holds in ridx[q] the row of stage 2q + (l >> 4), K row
-      // 2 * warp + (l & 1) + 8 * ((l >> 1) & 7) of that stage.
-      int ridx[4] = {0, 0, 0, 0};
-      if (!MN) {
+      size_t roff[GATHER && !MN ? NIK : 1];
+      if (GATHER && !MN) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int m = mt * kTileM + r8 + 16 * i;
-          const int r = m < count ? (g.rows ? ld_dep(g.rows + m) : m) : 0;
-          roff[i] = (size_t)r * g.lda * 2 + (size_t)j8 * 16;
+        for (int i = 0; i < NIK; ++i) {
+          const int m = mt * kTileM + tid / TPR + RPI * i;
+          const int r = m < count ? ld_dep(g.rows + m) : 0;
+          roff[i] = (size_t)r * g.lda * 2 + (size_t)(tid % TPR) * 16;
         }
       }
+      int nidx = 0;  // MN-major: this lane's row of the next stage
+      if (GATHER && MN && li < NIM) {
+        const int kidx = kb0 * kTileK + k0 + RPK * li;
+        nidx = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
+      }
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        if (MN && ((kb - kb0) & 7) == 0) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int kidx = (kb + 2 * q + (lane >> 4)) * kTileK + 2 * warp + (lane & 1) + 8 * ((lane >> 1) & 7);
-            ridx[q] = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
-          }
-        }
         const int s = it % stages;
-        const bool ok = __all_sync(SFFN_FULL_MASK,
-                                   it < stages || mbar_wait_bounded(&empty[s], (uint32_t)((it / stages - 1) & 1)));
-        if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
+        bool ok = it < stages || mbar_wait_bounded(&empty[s], (uint32_t)((it / stages - 1) & 1));
+        if (GATHER) ok = __all_sync(SFFN_FULL_MASK, ok);
+        const bool stop = GATHER ? __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)
+                                 : (*(volatile int*)&s_abort != 0);
+        if (!ok || stop) {
           if (!ok && lane == 0) {
             set_device_error(g.err, SFFN_ERR_TIMEOUT);
             atomicExch(&s_abort, 1);
@@ -180,41 +231,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
           goto producers_done;
         }
         unsigned char* st = ring + (size_t)s * kStage;
-        if (!MN) {
-          const size_t kofs = (size_t)kb * kTileK * 2;
+        unsigned char* sb = st + kATiles * kA;
+        if (tid == 0) {
+          mbar_arrive_expect_tx(&tfull[s], KSUB * ((GATHER ? 0u : kA) + kBt));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t so = tc::kmajor_off(r8 + 16 * i, j8);
-            tc::cp_async16(st + so, g.A0 + roff[i] + kofs);
-            if (NMAT == 2) tc::cp_async16(st + kA + so, g.A1 + roff[i] + kofs);
-          }
-        } else {
-          const int sc = (kb - kb0) & 7;  // stage within the eight held in ridx
-          const int q = sc >> 1;
-          const int v = q == 0 ? ridx[0] : (q == 1 ? ridx[1] : (q == 2 ? ridx[2] : ridx[3]));
-          const size_t mofs = ((size_t)mt * kTileM + c16 * 8) * 2;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = __shfl_sync(SFFN_FULL_MASK, v, ((sc & 1) << 4) | (i << 1) | (lane >> 4));
-            tc::cp_async16(st + tc::mnmajor_off(k16 + 8 * i, c16), g.A0 + (size_t)r * g.lda * 2 + mofs);
+          for (int j = 0; j < KSUB; ++j) {
+            const int kx = (kb * KSUB + j) * kTileK;
+            if (!GATHER) tc::tma_load_2d(st + j * kA, &g.tmA, kx, mt * kTileM, &tfull[s], pol_a);
+            tc::tma_load_2d(sb + j * kBt, &g.tmB, kx, 0, &tfull[s], pol_b);
           }
         }
-        // B: hi and lo parts, NPAD rows x 8 chunks each
-        unsigned char* sb = st + NMAT * kA;
+        if (GATHER) {
+          if (!MN) {
+            const int c = tid % TPR, jb = c >> 3, cj = c & 7;
+            const size_t kofs = (size_t)kb * KSUB * kTileK * 2;
 #pragma unroll
-        for (int idx = tid; idx < 2 * NPAD * 8; idx += kProducers) {
-          const int hl = idx / (NPAD * 8), n = (idx / 8) % NPAD, j = idx % 8;
-          tc::cp_async16(sb + hl * kB + tc::kmajor_off(n, j),
-                         g.Bhl + (((size_t)hl * NPAD + n) * g.ldb + (size_t)kb * kTileK + j * 8) * 2);
+            for (int i = 0; i < NIK; ++i) {
+              const uint32_t so = (uint32_t)(jb * NMAT) * kA + tc::kmajor_off(tid / TPR + RPI * i, cj);
+              tc::cp_async16(st + so, g.A0 + roff[i] + kofs);
+              if (NMAT == 2) tc::cp_async16(st + so + kA, g.A1 + roff[i] + kofs);
+            }
+          } else {
+            const int cur = nidx;
+            if (kb + 1 < kb1 && li < NIM) {  // the next stage's rows, loaded while this one streams
+              const int kidx = (kb + 1) * kTileK + k0 + RPK * li;
+              nidx = ld_dep(g.rows + (kidx < count ? kidx : count - 1));
+            }
+            const int c = tid % TPK, mi = c >> 4, c16 = c & 15;
+            const size_t mofs = ((size_t)mt * MSUB * kTileM + (size_t)mi * kTileM + c16 * 8) * 2;
+#pragma unroll
+            for (int i = 0; i < NIM; ++i) {
+              const int r = __shfl_sync(SFFN_FULL_MASK, cur, hbase | i);
+              tc::cp_async16(st + mi * kA + tc::mnmajor_off(k0 + RPK * i, c16), g.A0 + (size_t)r * g.lda * 2 + mofs);
+            }
+          }
+          tc::cp_async_arrive(&full[s]);
         }
-        tc::cp_async_arrive(&full[s]);
       }
     }
   producers_done:
-    tc::cp_async_wait_all();
-  } else {
+    if (GATHER) tc::cp_async_wait_all();
+    // let this CTA's TMA loads that no MMA consumed land before exiting
+    if (tid == 0 && *(volatile int*)&s_abort)
+      for (int q = it > stages ? it - stages : 0; q < it; ++q)
+        mbar_wait_bounded(&tfull[q % stages], (uint32_t)((q / stages) & 1));
+  } else if (warp >= 4) {
     // ------------------------------------------------- MMA issue + epilogue
-    const uint32_t idesc = tc::instr_desc(bf16, MN, NPAD);
+    const uint32_t idesc = tc::instr_desc(bf16, MN, N2);
     const int ew = warp - 4;  // TMEM lane quarter of this warp
     int it = 0, ui = 0;
     bool issued = false;
@@ -226,22 +289,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
         if (ok) tc::fence_after();
         for (int kb = kb0; ok && kb < kb1; ++kb, ++it) {
           const int s = it % stages;
-          ok = mbar_wait_bounded(&full[s], (uint32_t)((it / stages) & 1));
+          ok = mbar_wait_bounded(&tfull[s], (uint32_t)((it / stages) & 1));
+          if (ok && GATHER) ok = mbar_wait_bounded(&full[s], (uint32_t)((it / stages) & 1));
           if (!ok || *(volatile int*)&s_abort) break;
-          fence_proxy_async_smem();  // cp.async writes -> tensor core reads
+          if (GATHER) fence_proxy_async_smem();  // cp.async writes -> tensor core reads
           tc::fence_after();
-          const uint32_t sa = smem_u32(ring + (size_t)s * kStage);
-          const uint32_t sb = sa + NMAT * kA;
+          const uint32_t sa0 = smem_u32(ring + (size_t)s * kStage);
+          const uint32_t sb0 = sa0 + kATiles * kA;
 #pragma unroll
-          for (int step = 0; step < 4; ++step) {
+          for (int j = 0; j < KSUB; ++j) {
 #pragma unroll
-            for (int a = 0; a < NMAT; ++a) {
-              const uint64_t ad = MN ? tc::smem_desc(sa + step * 4096, 1024, 2048)
-                                     : tc::smem_desc(sa + a * kA + step * 32, 16, 1024);
+            for (int step = 0; step < 4; ++step) {
+              const uint64_t bd = tc::smem_desc(sb0 + j * kBt + step * 32, 16, 1024);
 #pragma unroll
-              for (int hl = 0; hl < 2; ++hl) {
-                const uint64_t bd = tc::smem_desc(sb + hl * kB + step * 32, 16, 1024);
-                tc::mma(tmem + a * NPAD, ad, bd, idesc, !(kb == kb0 && step == 0 && hl == 0));
+              for (int a = 0; a < NACC; ++a) {
+                const uint64_t ad = MN ? tc::smem_desc(sa0 + a * kA + step * 4096, 1024, 2048)
+                                       : tc::smem_desc(sa0 + (j * NMAT + a) * kA + step * 32, 16, 1024);
+                tc::mma(tmem + a * N2, ad, bd, idesc, !(kb == kb0 && j == 0 && step == 0));
               }
             }
           }
@@ -256,7 +320,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
         issued = true;
       }
       __syncwarp();
-      // epilogue: every warp of 4..7 reads its 32 rows of each accumulator
+      // epilogue: every warp of 4..7 reads its 32 rows of each accumulator and
+      // adds the lo half of the columns to the hi half
       const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(dfull, (uint32_t)(ui & 1)));
       if (!ok || __any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
         if (!ok && lane == 0) {
@@ -266,18 +331,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_tc_gemm(GemmArgs g, bool bf
         break;
       }
       tc::fence_after();
-      const size_t row = (size_t)(cta + mt) * kTileM + ew * 32 + lane;  // slot cta + mt
+      const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16);
 #pragma unroll
-      for (int a = 0; a < NMAT; ++a) {
-        float* dst = g.D + (size_t)a * g.dmat_stride + row * NPAD;
+      for (int a = 0; a < NACC; ++a) {
+        // slot cta + mt; MN-major: row a * 128 + r of the slot's MSUB * 128 rows
+        float* dst = MN ? g.D + ((size_t)(cta + mt) * p.tile_rows + a * kTileM + ew * 32 + lane) * NPAD
+                        : g.D + (size_t)a * g.dmat_stride + ((size_t)(cta + mt) * kTileM + ew * 32 + lane) * NPAD;
 #pragma unroll
         for (int c0 = 0; c0 < NPAD; c0 += 16) {
-          float v[16];
-          tc::ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * NPAD + c0), v);
+          float vh[16], vl[16];
+          tc::ld16(tl + (uint32_t)(a * N2 + c0), vh);
+          tc::ld16(tl + (uint32_t)(a * N2 + NPAD + c0), vl);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            *reinterpret_cast<float4*>(dst + c0 + i) =
+                make_float4(vh[i] + vl[i], vh[i + 1] + vl[i + 1], vh[i + 2] + vl[i + 2], vh[i + 3] + vl[i + 3]);
         }
       }
       tc::fence_before();
@@ -329,7 +398,7 @@ __global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
   }
 }
 
-// The partial tiles are laid out [slot][128][npad]: one row's npad values
+// The partial tiles are laid out [slot][tile_rows][npad]: one row's npad values
 // are contiguous, so the finishers below give each thread four tokens of one
 // row (a 16-byte load per partial) and let consecutive threads take
 // consecutive rows, which keeps their 16-bit outputs [npad][rows] coalesced.
@@ -339,10 +408,10 @@ __global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
 __device__ __forceinline__ float4 sum_segments(const float* D, const Plan& p, int row, int npad, int nq) {
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.total == 0) return a;
-  const int mt = row / kTileM, rr = row % kTileM;
+  const int mt = row / p.tile_rows, rr = row % p.tile_rows;
   const int b0 = cta_of(p, (long long)mt * p.kblocks), b1 = cta_of(p, (long long)(mt + 1) * p.kblocks - 1);
   for (int b = b0; b <= b1; ++b) {
-    const float4 v = ld_dep4(D + ((size_t)(b + mt) * kTileM + rr) * npad + nq * 4);
+    const float4 v = ld_dep4(D + ((size_t)(b + mt) * p.tile_rows + rr) * npad + nq * 4);
     a.x += v.x;
     a.y += v.y;
     a.z += v.z;
@@ -364,7 +433,7 @@ __global__ void k_b_hidden_fin(const float* D, int d, int grid, int npad, int h,
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (npad / 4) * h) return;
   const int nq = i / h, j = i % h;
-  const Plan p = make_plan(false, h, d, grid);  // the hidden product's plan (K = d)
+  const Plan p = make_plan(false, h, d, grid, ksub_contig(d));  // the hidden product's plan (K = d)
   const float4 a = sum_segments(D, p, j, npad, nq);
   const float bias = b1 ? b1[j] : 0.f;
 #pragma unroll
@@ -389,7 +458,7 @@ __global__ void k_b_scores_fin(const float* D, int h, int grid, int npad, int nw
   const int nq = gw / nw, w = gw % nw;
   if (nq >= npad / 4 || nq * 4 >= B) return;
   const int row = w * 32 + lane;
-  const Plan p = make_plan(false, nw * 32, h, grid);  // the scores product's plan (K = h)
+  const Plan p = make_plan(false, nw * 32, h, grid, ksub_contig(h));  // the scores product's plan (K = h)
   const float4 a = sum_segments(D, p, row, npad, nq);
   const float bias = b2 ? b2[row] : 0.f;
   uint32_t mine = 0;
@@ -455,7 +524,7 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
   const int U = ld_dep(ucount);
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (u < U && nq * 4 < B) {
-    const Plan p = make_plan(false, U, d, grid);  // the up/gate product's plan (K = d)
+    const Plan p = make_plan(false, U, d, grid, ksub_gather(d, ACT != SFFN_ACT_RELU ? 2 : 1));  // the up/gate plan
     const float4 au = sum_segments(Du, p, u, npad, nq);
     const float4 ag = ACT != SFFN_ACT_RELU ? sum_segments(Dg, p, u, npad, nq) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int slot = ld_dep(uidx + u);
@@ -487,7 +556,7 @@ __global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad
   const int nq = i / d, c = i % d;
   if (nq * 4 >= B) return;
   const int U = ld_dep(ucount);
-  const Plan p = make_plan(true, U, d, grid);
+  const Plan p = make_plan(true, U, d, grid, 1, msub_down(d));
   const float4 a = sum_segments(D, p, c, npad, nq);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -514,39 +583,111 @@ size_t rows_bound(const sffn_layer& L, int m_tiles_max) {
   return ((size_t)gemm_grid(L) + (size_t)m_tiles_max) * kTileM;  // partial slots < CTAs + tiles
 }
 
-template <bool MN, int NMAT, int NPAD>
-size_t gemm_smem(int stages) {
-  const size_t stage = (size_t)NMAT * kTileM * kTileK * 2 + 2 * (size_t)NPAD * kTileK * 2;
-  return 1024 + (size_t)stages * stage + (size_t)(2 * stages + 3) * 8;
+template <bool MN, int NMAT, int NPAD, int KSUB, int MSUB>
+size_t gemm_stage_bytes() {
+  const size_t a_tiles = MN ? MSUB : (size_t)KSUB * NMAT;
+  return a_tiles * kTileM * kTileK * 2 + (size_t)KSUB * 2 * NPAD * kTileK * 2;
 }
 
-template <bool MN, int NMAT, int NPAD>
+template <bool MN, int NMAT, int NPAD, int KSUB, int MSUB>
 int gemm_stages() {
-  const size_t stage = (size_t)NMAT * kTileM * kTileK * 2 + 2 * (size_t)NPAD * kTileK * 2;
-  return (int)std::min<size_t>(8, (kGemmSmemBudget - 2048) / stage);
+  return (int)std::min<size_t>(8, (kGemmSmemBudget - 2048) / gemm_stage_bytes<MN, NMAT, NPAD, KSUB, MSUB>());
 }
 
-template <bool MN, int NMAT, int NPAD>
-cudaError_t set_gemm_attr() {
-  const size_t smem = gemm_smem<MN, NMAT, NPAD>(gemm_stages<MN, NMAT, NPAD>());
-  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<MN, NMAT, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+template <bool MN, int NMAT, int NPAD, int KSUB, int MSUB>
+size_t gemm_smem() {
+  const int stages = gemm_stages<MN, NMAT, NPAD, KSUB, MSUB>();
+  return 1024 + (size_t)stages * gemm_stage_bytes<MN, NMAT, NPAD, KSUB, MSUB>() + (size_t)(3 * stages + 3) * 8;
+}
+
+template <bool MN, int NMAT, int NPAD, int KSUB, int MSUB>
+constexpr bool gemm_stage_bytes_ok() {
+  return 2 * ((MN ? MSUB : KSUB * NMAT) * kTileM * kTileK * 2 + KSUB * 2 * NPAD * kTileK * 2) <= kGemmSmemBudget - 2048;
+}
+
+template <bool MN, int NMAT, int NPAD, bool GATHER, int KSUB, int MSUB>
+cudaError_t set_gemm_attr_one() {
+  static_assert(gemm_stage_bytes_ok<MN, NMAT, NPAD, KSUB, MSUB>(), "two ring stages must fit");
+  auto* k = k_tc_gemm<MN, NMAT, NPAD, GATHER, KSUB, MSUB>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemm_smem<MN, NMAT, NPAD, KSUB, MSUB>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_tc_gemm<MN, NMAT, NPAD>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
-template <bool MN, int NMAT, int NPAD>
-cudaError_t launch_gemm(const sffn_layer& L, const GemmArgs& g, cudaStream_t st) {
-  const int stages = gemm_stages<MN, NMAT, NPAD>();
-  const size_t smem = gemm_smem<MN, NMAT, NPAD>(stages);
-  return launch_ex(k_tc_gemm<MN, NMAT, NPAD>, dim3(g.grid), dim3(kGemmThreads), smem, st, true, 1, g,
-                   L.desc.wdtype == SFFN_BF16, stages);
+template <bool MN, int NMAT, bool GATHER, int KSUB, int MSUB>
+cudaError_t set_gemm_attr() {
+  cudaError_t e = set_gemm_attr_one<MN, NMAT, 16, GATHER, KSUB, MSUB>();
+  return e != cudaSuccess ? e : set_gemm_attr_one<MN, NMAT, 32, GATHER, KSUB, MSUB>();
 }
 
-template <bool MN, int NMAT>
-cudaError_t launch_gemm_n(const sffn_layer& L, int npad, const GemmArgs& g, cudaStream_t st) {
-  return npad == 16 ? launch_gemm<MN, NMAT, 16>(L, g, st) : launch_gemm<MN, NMAT, 32>(L, g, st);
+template <bool MN, int NMAT, bool GATHER, int KSUB, int MSUB>
+cudaError_t launch_gemm(const sffn_layer& L, int npad, const GemmArgs& g, cudaStream_t st) {
+  const bool bf = L.desc.wdtype == SFFN_BF16;
+  if (npad == 16)
+    return launch_ex(k_tc_gemm<MN, NMAT, 16, GATHER, KSUB, MSUB>, dim3(g.grid), dim3(kGemmThreads),
+                     gemm_smem<MN, NMAT, 16, KSUB, MSUB>(), st, true, 1, g, bf,
+                     gemm_stages<MN, NMAT, 16, KSUB, MSUB>());
+  return launch_ex(k_tc_gemm<MN, NMAT, 32, GATHER, KSUB, MSUB>, dim3(g.grid), dim3(kGemmThreads),
+                   gemm_smem<MN, NMAT, 32, KSUB, MSUB>(), st, true, 1, g, bf, gemm_stages<MN, NMAT, 32, KSUB, MSUB>());
+}
+
+// Contiguous rows (hidden, scores): K steps of ksub_contig(K) blocks.
+cudaError_t launch_contig(const sffn_layer& L, int npad, const GemmArgs& g, cudaStream_t st) {
+  return ksub_contig(g.other) == 4 ? launch_gemm<false, 1, false, 4, 1>(L, npad, g, st)
+                                   : launch_gemm<false, 1, false, 1, 1>(L, npad, g, st);
+}
+
+// Gathered union rows of up (and gate): K steps of ksub_gather(d, nmat) blocks.
+cudaError_t launch_upgate(const sffn_layer& L, int npad, bool gated, const GemmArgs& g, cudaStream_t st) {
+  const int ks = ksub_gather(g.other, gated ? 2 : 1);
+  if (gated) return ks == 2 ? launch_gemm<false, 2, true, 2, 1>(L, npad, g, st)
+                            : launch_gemm<false, 2, true, 1, 1>(L, npad, g, st);
+  return ks == 4 ? launch_gemm<false, 1, true, 4, 1>(L, npad, g, st)
+                 : (ks == 2 ? launch_gemm<false, 1, true, 2, 1>(L, npad, g, st)
+                            : launch_gemm<false, 1, true, 1, 1>(L, npad, g, st));
+}
+
+// Gathered union rows of downT (MN-major): output tiles of msub_down(d) x 128 rows.
+cudaError_t launch_down(const sffn_layer& L, int npad, const GemmArgs& g, cudaStream_t st) {
+  const int ms = msub_down(g.other);
+  return ms == 4 ? launch_gemm<true, 1, true, 1, 4>(L, npad, g, st)
+                 : (ms == 2 ? launch_gemm<true, 1, true, 1, 2>(L, npad, g, st)
+                            : launch_gemm<true, 1, true, 1, 1>(L, npad, g, st));
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a row-major 16-bit matrix [rows][inner] (row pitch
+// inner * 2 bytes, a multiple of 16) read in boxes of 64 x box_rows elements
+// with the 128-byte swizzle. Rows past the end read as zero.
+cudaError_t encode_rows(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t rows,
+                        uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -572,7 +713,8 @@ BatchWs batch_ws_layout(const sffn_layer& L, int B) {
   w.ucount = take(256);
   w.dug = take(2 * rows_bound(L, (int)((f + kTileM - 1) / kTileM)) * npad * 4);
   w.hhl = take(2 * npad * fpad * 2);
-  w.dy = take(rows_bound(L, (int)(d / kTileM)) * npad * 4);
+  // down partials: slots < CTAs + tiles, tile_rows = msub_down(d) * 128
+  w.dy = take(((size_t)gemm_grid(L) * kTileM * msub_down((int)d) + d) * npad * 4);
   w.total = off;
   return w;
 }
@@ -592,12 +734,17 @@ bool batch_supported(const sffn_layer& L, std::string* why) {
 cudaError_t configure_batch_kernels(const sffn_layer& L) {
   if (!batch_supported(L, nullptr)) return cudaSuccess;
   cudaError_t e;
-  if ((e = set_gemm_attr<false, 1, 16>())) return e;
-  if ((e = set_gemm_attr<false, 1, 32>())) return e;
-  if ((e = set_gemm_attr<false, 2, 16>())) return e;
-  if ((e = set_gemm_attr<false, 2, 32>())) return e;
-  if ((e = set_gemm_attr<true, 1, 16>())) return e;
-  return set_gemm_attr<true, 1, 32>();
+  if (!tensor_map_encoder()) return cudaErrorNotSupported;
+  if ((e = set_gemm_attr<false, 1, false, 1, 1>())) return e;
+  if ((e = set_gemm_attr<false, 1, false, 4, 1>())) return e;
+  if ((e = set_gemm_attr<false, 1, true, 1, 1>())) return e;
+  if ((e = set_gemm_attr<false, 1, true, 2, 1>())) return e;
+  if ((e = set_gemm_attr<false, 1, true, 4, 1>())) return e;
+  if ((e = set_gemm_attr<false, 2, true, 1, 1>())) return e;
+  if ((e = set_gemm_attr<false, 2, true, 2, 1>())) return e;
+  if ((e = set_gemm_attr<true, 1, true, 1, 1>())) return e;
+  if ((e = set_gemm_attr<true, 1, true, 1, 2>())) return e;
+  return set_gemm_attr<true, 1, true, 1, 4>();
 }
 
 // Records the layer's trace event for slot k (if any) around `launch`.
@@ -646,7 +793,9 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     g.D = reinterpret_cast<float*>(base + w.dh);
     g.grid = grid;
     g.err = L.err;
-    e = traced_b(L, 0, st, [&] { return launch_gemm_n<false, 1>(L, npad, g, st); });
+    e = encode_rows(&g.tmA, L.W1, bf, d, h, kTileM);
+    if (e == cudaSuccess) e = encode_rows(&g.tmB, xhl, bf, d, 2 * npad, 2 * npad);
+    if (e == cudaSuccess) e = traced_b(L, 0, st, [&] { return launch_contig(L, npad, g, st); });
     if (e != cudaSuccess) return e;
     void* hidhl = base + w.hidhl;
     const int hb = ((npad / 4) * h + 255) / 256;
@@ -670,7 +819,9 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     s.D = reinterpret_cast<float*>(base + w.ds);
     s.grid = grid;
     s.err = L.err;
-    e = traced_b(L, 1, st, [&] { return launch_gemm_n<false, 1>(L, npad, s, st); });
+    e = encode_rows(&s.tmA, L.W2, bf, h, f, kTileM);
+    if (e == cudaSuccess) e = encode_rows(&s.tmB, hidhl, bf, h, 2 * npad, 2 * npad);
+    if (e == cudaSuccess) e = traced_b(L, 1, st, [&] { return launch_contig(L, npad, s, st); });
     if (e != cudaSuccess) return e;
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
     e = launch_ex(k_b_scores_fin, dim3((nw * (npad / 4) + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
@@ -700,9 +851,8 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   u.dmat_stride = dmat;
   u.grid = grid;
   u.err = L.err;
-  e = traced_b(L, 2, st, [&] {
-    return gated ? launch_gemm_n<false, 2>(L, npad, u, st) : launch_gemm_n<false, 1>(L, npad, u, st);
-  });
+  e = encode_rows(&u.tmB, xhl, bf, d, 2 * npad, 2 * npad);
+  if (e == cudaSuccess) e = traced_b(L, 2, st, [&] { return launch_upgate(L, npad, gated, u, st); });
   if (e != cudaSuccess) return e;
   // activation with each token's own mask -> H parts [2][npad][fpad]
   void* hhl = base + w.hhl;
@@ -731,7 +881,8 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.D = reinterpret_cast<float*>(base + w.dy);
   dn.grid = grid;
   dn.err = L.err;
-  e = traced_b(L, 3, st, [&] { return launch_gemm_n<true, 1>(L, npad, dn, st); });
+  e = encode_rows(&dn.tmB, hhl, bf, fpad, 2 * npad, 2 * npad);
+  if (e == cudaSuccess) e = traced_b(L, 3, st, [&] { return launch_down(L, npad, dn, st); });
   if (e != cudaSuccess) return e;
   return launch_ex(k_b_y_fin, dim3(((npad / 4) * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
                    static_cast<const int32_t*>(ucount), d, npad, B, grid, x, y, x_out);

@@ -97,6 +97,25 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Two-dimensional tiled TMA load of the box at element coordinates (x, y) of
+// the tensor map into shared memory at dst (1024-byte aligned for the
+// 128-byte swizzle); completion is signalled on `bar` as transaction bytes.
+// x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Byte offset of 16-byte chunk j (0..7) of row r in a K-major 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t kmajor_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) * 16)); }
 
