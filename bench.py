@@ -78,6 +78,39 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# DRAM counters of one kernel, taken by ncu on a named capture and stored
+# beside its summary in profiles/; valid only while the kernel's sources hash
+# to the value recorded with them.
+TRAFFIC_FILES = {"ffn": "profiles/k_ffn_dram_traffic.json"}
+
+
+def sources_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, units_per_launch: float, prefetch: bool):
+    """DRAM bytes (read + write) per launch of `kernel` at `units_per_launch`
+    active neurons, scaled from the stored capture by units processed (the
+    kernel's traffic grows with the active rows it streams), plus the
+    next-layer W1 prefetch when the L2 hint is on; or None."""
+    rel = TRAFFIC_FILES.get(kernel)
+    if rel is None or not os.path.exists(os.path.join(ROOT, rel)):
+        return None
+    with open(os.path.join(ROOT, rel)) as fh:
+        d = json.load(fh)
+    if sources_sha256(d["sources"]) != d["sources_sha256"]:
+        return None   # the kernel changed since the counters were taken
+    l0 = d["launches"][0]
+    fixed = d.get("l2_prefetch_bytes_per_launch", 0) if prefetch else 0
+    per_unit = (l0["dram_read"] + l0["dram_write"] - d.get("l2_prefetch_bytes_per_launch", 0)) / l0["active_neurons"]
+    return per_unit * units_per_launch + fixed
+
+
 def measured_tensor_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -499,6 +532,9 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peaks()
     pk = per_kernel[dom]
     dom_traffic = None
+    if Bt == 1:
+        t = measured_traffic(dom, float(counts.mean()), prefetch_next)
+        dom_traffic = round(t) if t is not None else None
     active_frac = float(tok_counts.mean() / Bt / spec.f)
     line = {
         "metric": METRIC,
@@ -542,6 +578,7 @@ def run_ours(args, world, rank, local):
     }
     if replicas_note:
         line["config"]["replicas"] = replicas_note
+    line["census"] = {"distinct_tokens": P, "active_count_token0_by_layer": [int(c) for c in counts[0]]}
     if Bt > 1:
         line["union_frac"] = round(float(counts.mean() / spec.f), 5)
         tpk, _ = measured_tensor_peak()
