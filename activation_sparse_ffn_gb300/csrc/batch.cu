@@ -103,6 +103,8 @@ __host__ __device__ inline int msub_down(int d) {
   return t % 4 == 0 ? 4 : (t % 2 == 0 ? 2 : 1);
 }
 
+__host__ __device__ inline bool cta_in_plan(const Plan& p, int b) { return b < p.ctas; }
+
 // First linear (tile, K step) index of CTA b's range.
 __host__ __device__ inline long long range_lo(const Plan& p, int b) { return p.total * b / p.ctas; }
 
@@ -172,6 +174,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = s_tmem;
 
   pdl_launch_dependents();
+  // Contiguous products: the weights are not written by earlier kernels, so
+  // thread 0 requests the A tiles of this CTA's first ring stages before the
+  // wait; their B tiles (written by the previous kernel) follow after it. The
+  // stage's barrier is told the bytes of both at once.
+  int pre = 0;
+  if (!GATHER && tid == 0) {
+    const Plan p0 = make_plan(false, g.fixed_count, g.other, g.grid, KSUB, 1);
+    if (cta_in_plan(p0, blockIdx.x)) {
+      const uint64_t pol_a = l2_policy_evict_first();
+      const long long i_lo = range_lo(p0, blockIdx.x), i_hi = range_lo(p0, blockIdx.x + 1);
+      for (; pre < stages && i_lo + pre < i_hi; ++pre) {
+        const long long i = i_lo + pre;
+        const int mt = (int)(i / p0.kblocks), kb = (int)(i % p0.kblocks);
+        unsigned char* st = ring + (size_t)pre * kStage;
+        mbar_arrive_expect_tx(&tfull[pre], KSUB * (kA + kBt));
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j)
+          tc::tma_load_2d(st + j * kA, &g.tmA, (kb * KSUB + j) * kTileK, mt * kTileM, &tfull[pre], pol_a);
+      }
+    }
+  }
   pdl_wait();  // operands and row lists come from earlier kernels
   const int count = g.count_dev ? ld_dep(g.count_dev) : g.fixed_count;
   const Plan p = make_plan(MN, count, g.other, g.grid, KSUB, MSUB);
@@ -233,11 +256,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         unsigned char* st = ring + (size_t)s * kStage;
         unsigned char* sb = st + kATiles * kA;
         if (tid == 0) {
-          mbar_arrive_expect_tx(&tfull[s], KSUB * ((GATHER ? 0u : kA) + kBt));
+          const bool early = it < pre;  // A tiles already requested before the wait
+          if (!early) mbar_arrive_expect_tx(&tfull[s], KSUB * ((GATHER ? 0u : kA) + kBt));
 #pragma unroll
           for (int j = 0; j < KSUB; ++j) {
             const int kx = (kb * KSUB + j) * kTileK;
-            if (!GATHER) tc::tma_load_2d(st + j * kA, &g.tmA, kx, mt * kTileM, &tfull[s], pol_a);
+            if (!GATHER && !early) tc::tma_load_2d(st + j * kA, &g.tmA, kx, mt * kTileM, &tfull[s], pol_a);
             tc::tma_load_2d(sb + j * kBt, &g.tmB, kx, 0, &tfull[s], pol_b);
           }
         }
@@ -272,9 +296,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   producers_done:
     if (GATHER) tc::cp_async_wait_all();
     // let this CTA's TMA loads that no MMA consumed land before exiting
-    if (tid == 0 && *(volatile int*)&s_abort)
-      for (int q = it > stages ? it - stages : 0; q < it; ++q)
+    if (tid == 0 && *(volatile int*)&s_abort) {
+      const int n = it > pre ? it : pre;
+      for (int q = n > stages ? n - stages : 0; q < n; ++q)
         mbar_wait_bounded(&tfull[q % stages], (uint32_t)((q / stages) & 1));
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------- MMA issue + epilogue
     const uint32_t idesc = tc::instr_desc(bf16, MN, N2);
@@ -410,6 +436,7 @@ __device__ __forceinline__ float4 sum_segments(const float* D, const Plan& p, in
   if (p.total == 0) return a;
   const int mt = row / p.tile_rows, rr = row % p.tile_rows;
   const int b0 = cta_of(p, (long long)mt * p.kblocks), b1 = cta_of(p, (long long)(mt + 1) * p.kblocks - 1);
+#pragma unroll 4
   for (int b = b0; b <= b1; ++b) {
     const float4 v = ld_dep4(D + ((size_t)(b + mt) * p.tile_rows + rr) * npad + nq * 4);
     a.x += v.x;
