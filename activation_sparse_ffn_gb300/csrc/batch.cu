@@ -436,7 +436,7 @@ __device__ __forceinline__ float4 sum_segments(const float* D, const Plan& p, in
   if (p.total == 0) return a;
   const int mt = row / p.tile_rows, rr = row % p.tile_rows;
   const int b0 = cta_of(p, (long long)mt * p.kblocks), b1 = cta_of(p, (long long)(mt + 1) * p.kblocks - 1);
-#pragma unroll 4
+#pragma unroll 8
   for (int b = b0; b <= b1; ++b) {
     const float4 v = ld_dep4(D + ((size_t)(b + mt) * p.tile_rows + rr) * npad + nq * 4);
     a.x += v.x;
@@ -474,35 +474,40 @@ __global__ void k_b_hidden_fin(const float* D, int d, int grid, int npad, int h,
   }
 }
 
-// nmask[n][w] for every token n < B: one warp per (mask word, token quad),
-// lane = row of the word, one ballot per token.
+// nmask[n][w] for every token n < B, and the union word unmask[w]: one warp
+// per mask word, lane = row of the word, one ballot per token.
 __global__ void k_b_scores_fin(const float* D, int h, int grid, int npad, int nw, int B, const float* b2,
-                               float thres, uint32_t* nmask) {
+                               float thres, uint32_t* nmask, uint32_t* unmask) {
   pdl_launch_dependents();
   pdl_wait();
-  const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
-  const int nq = gw / nw, w = gw % nw;
-  if (nq >= npad / 4 || nq * 4 >= B) return;
+  if (w >= nw) return;
   const int row = w * 32 + lane;
   const Plan p = make_plan(false, nw * 32, h, grid, ksub_contig(h));  // the scores product's plan (K = h)
-  const float4 a = sum_segments(D, p, row, npad, nq);
   const float bias = b2 ? b2[row] : 0.f;
-  uint32_t mine = 0;
+  uint32_t mine = 0, uni = 0;
+  for (int nq = 0; nq * 4 < B; ++nq) {
+    const float4 a = sum_segments(D, p, row, npad, nq);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t m = __ballot_sync(SFFN_FULL_MASK, f4_get(a, e) + bias >= thres);  // NaN compares false
-    if (lane == e) mine = m;
+    for (int e = 0; e < 4; ++e) {
+      const int n = nq * 4 + e;
+      const uint32_t m = __ballot_sync(SFFN_FULL_MASK, n < B && f4_get(a, e) + bias >= thres);  // NaN: false
+      if (lane == n) mine = m;
+      uni |= m;
+    }
   }
-  const int n = nq * 4 + lane;
-  if (lane < 4 && n < B) nmask[(size_t)n * nw + w] = mine;
+  if (lane < B) nmask[(size_t)lane * nw + w] = mine;
+  if (lane == 0) unmask[w] = uni;
 }
 
 // Views: block b < B expands token b's mask (index list, count, group mask);
-// block B forms the union mask (OR over tokens) and its views.
+// block B expands the union mask, forming it first (OR over tokens) unless
+// the scores finisher already wrote it (union_ready).
 __global__ void __launch_bounds__(kViewThreadsB)
     k_b_views(const uint32_t* nmask, int B, int nw, int f, int n_groups, int G, int gwords, int32_t* idx,
-              int32_t* count, uint32_t* gmask, uint32_t* unmask, int32_t* uidx, int32_t* ucount, uint32_t* ugmask) {
+              int32_t* count, uint32_t* gmask, uint32_t* unmask, int32_t* uidx, int32_t* ucount, uint32_t* ugmask,
+              bool union_ready) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem[];
@@ -513,6 +518,8 @@ __global__ void __launch_bounds__(kViewThreadsB)
   const uint32_t* src;
   if (b < B) {
     src = nmask + (size_t)b * nw;
+  } else if (union_ready) {
+    src = unmask;
   } else {
     // union words into the union mask output, then scanned like any token
     for (int w = threadIdx.x; w < nw; w += kViewThreadsB) {
@@ -549,6 +556,7 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
   if (i >= (npad / 4) * ldh) return;
   const int nq = i / ldh, u = i % ldh;
   const int U = ld_dep(ucount);
+  if (u >= (U + kTileK - 1) / kTileK * kTileK) return;  // the down product reads no further
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (u < U && nq * 4 < B) {
     const Plan p = make_plan(false, U, d, grid, ksub_gather(d, ACT != SFFN_ACT_RELU ? 2 : 1));  // the up/gate plan
@@ -851,15 +859,15 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     if (e == cudaSuccess) e = traced_b(L, 1, st, [&] { return launch_contig(L, npad, s, st); });
     if (e != cudaSuccess) return e;
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
-    e = launch_ex(k_b_scores_fin, dim3((nw * (npad / 4) + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D),
-                  h, grid, npad, nw, B, b2, thres, m->nmask);
+    e = launch_ex(k_b_scores_fin, dim3((nw + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D), h,
+                  grid, npad, nw, B, b2, thres, m->nmask, unmask);
     if (e != cudaSuccess) return e;
   }
   // per-token views (when predicting) and the union mask with its views
   e = launch_ex(k_b_views, dim3(B + 1), dim3(kViewThreadsB), (size_t)nw * 8, st, true, 1,
                 static_cast<const uint32_t*>(m->nmask), B, nw, f, L.n_groups, L.desc.group_size, L.gwords,
                 predict ? m->idx : nullptr, predict ? m->count : nullptr, predict ? m->gmask : nullptr, unmask, uidx,
-                ucount, m->ugmask);
+                ucount, m->ugmask, predict);
   if (e != cudaSuccess || !forward) return e;
 
   // up/gate over the union rows: D[U x N] = {up, gate} . X^T over K = d
