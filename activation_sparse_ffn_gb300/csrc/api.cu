@@ -139,6 +139,8 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   L->gwords = (L->n_groups + 31) / 32;
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&L->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
   if (e != cudaSuccess) {
     delete L;
     return cuda_fail(e, "sffn_layer_create: device query");
@@ -227,6 +229,22 @@ sffn_status sffn_layer_set_trace(sffn_layer* L, const sffn_trace* t) {
     L->trace_begin[k] = t ? static_cast<cudaEvent_t>(t->begin[k]) : nullptr;
     L->trace_end[k] = t ? static_cast<cudaEvent_t>(t->end[k]) : nullptr;
   }
+  return SFFN_OK;
+}
+
+sffn_status sffn_layer_set_grid(sffn_layer* L, int32_t ffn_blocks, int32_t score_blocks) {
+  if (!L) return invalid("layer is NULL");
+  if (ffn_blocks < 0 || ffn_blocks > L->num_sms || score_blocks < 0 || score_blocks > L->num_sms)
+    return invalid("sffn_layer_set_grid: block counts must lie in [0, number of SMs]");
+  const int old_ffn = L->ffn_grid, old_stages = L->ffn_stages;
+  L->ffn_grid = ffn_blocks;
+  L->ffn_stages = ffn_stages_for(*L);  // the per-block neuron list grows as blocks get fewer
+  if (L->ffn_stages < 2 || ffn_smem(*L) + 1024 > (size_t)L->smem_optin) {
+    L->ffn_grid = old_ffn;
+    L->ffn_stages = old_stages;
+    return invalid("sffn_layer_set_grid: too few FFN blocks for this layer's shared-memory ring");
+  }
+  L->score_grid = score_blocks;
   return SFFN_OK;
 }
 

@@ -108,6 +108,18 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Raise a kernel's dynamic shared-memory limit to what the device allows next
+// to the kernel's own static shared memory. Kernel attributes are shared by
+// every layer in the process, so the limit is set to the device maximum
+// rather than to one layer's need.
+template <typename K>
+inline cudaError_t set_dynamic_smem_max(K* kern, int optin) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, kern);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)a.sharedSizeBytes);
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the stream
 // has completed and its writes are visible (a no-op without the launch
 // attribute); allow the next kernel to start launching.

@@ -312,7 +312,7 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
 
 template <typename K>
 cudaError_t set_big_smem(K* kern, size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_dynamic_smem_max(kern, (int)smem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
@@ -332,7 +332,8 @@ int ffn_cpt(const sffn_layer& L) {
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
 }
 
-int ffn_list_cap(const sffn_layer& L) { return (L.desc.f + L.num_sms - 1) / L.num_sms + 1; }
+int ffn_grid_of(const sffn_layer& L) { return L.ffn_grid > 0 ? L.ffn_grid : L.num_sms; }
+int ffn_list_cap(const sffn_layer& L) { return (L.desc.f + ffn_grid_of(L) - 1) / ffn_grid_of(L) + 1; }
 
 size_t ffn_fixed_smem(const sffn_layer& L) {
   const size_t cap = (size_t)ffn_list_cap(L);
@@ -343,7 +344,7 @@ size_t ffn_fixed_smem(const sffn_layer& L) {
 
 cudaError_t set_max_carveout();
 
-int ffn_blocks(const sffn_layer& L) { return L.num_sms; }
+int ffn_blocks(const sffn_layer& L) { return ffn_grid_of(L); }
 
 int ffn_stages_for(const sffn_layer& L) {
   const size_t stage = (size_t)L.desc.d * L.wbytes * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
@@ -356,8 +357,12 @@ size_t ffn_smem(const sffn_layer& L) {
   return (size_t)L.ffn_stages * (stage + 16) + ffn_fixed_smem(L);
 }
 
+// Kernel attributes are shared by every layer in the process, so the dynamic
+// shared-memory limit is raised to the device maximum once rather than to
+// this layer's need (a smaller layer created later must not lower it).
 cudaError_t configure_kernels(sffn_layer& L) {
-  const size_t sm = ffn_smem(L);
+  if (ffn_smem(L) + 1024 > (size_t)L.smem_optin) return cudaErrorInvalidConfiguration;
+  const size_t sm = (size_t)L.smem_optin;
   cudaError_t e = set_max_carveout();
   if (e != cudaSuccess) return e;
   switch (L.desc.wdtype) {

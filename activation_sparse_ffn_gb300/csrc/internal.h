@@ -14,6 +14,10 @@ struct sffn_layer {
   sffn_layer_desc desc;
   int device = 0;
   int num_sms = 0;
+  int smem_optin = 0;   // largest dynamic shared memory a block may request on this device
+  // B = 1 grid sizes (sffn_layer_set_grid); 0 = one block per SM
+  int ffn_grid = 0;
+  int score_grid = 0;
   int wbytes = 0;       // bytes per stored weight
   int n_groups = 0;
   int nwords = 0;       // f / 32

@@ -233,7 +233,7 @@ cudaError_t launch_hidden_t(const sffn_layer& L, const float* x, float* hid, cud
 
 template <typename T>
 cudaError_t launch_scores_t(const sffn_layer& L, const float* hid, float thres, uint32_t* nmask, cudaStream_t st) {
-  const dim3 grid(std::min(L.nwords, L.num_sms)), block(kScoreThreads);
+  const dim3 grid(std::min(L.nwords, L.score_grid > 0 ? L.score_grid : L.num_sms)), block(kScoreThreads);
   const float* b2 = L.has_b2 ? L.b2 : nullptr;
   return launch_ex(k_pred_scores<T>, grid, block, score_smem(L), st, true, 1, static_cast<const T*>(L.W2), b2, hid,
                    thres, nmask, L.desc.h, L.nwords, L.score_stages, L.err);
@@ -259,7 +259,7 @@ template <typename T>
 cudaError_t configure_predict_t(int sm) {
   // every hot kernel asks for the largest shared-memory carveout, so that
   // consecutive kernels of a decode step need no L1/shared reconfiguration
-  cudaError_t e = cudaFuncSetAttribute(k_pred_scores<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  cudaError_t e = set_dynamic_smem_max(k_pred_scores<T>, sm);
   if (e == cudaSuccess) e = carveout_max(k_pred_scores<T>);
   if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 1>);
   if (e == cudaSuccess) e = carveout_max(k_pred_hidden<T, 2>);
@@ -269,8 +269,10 @@ cudaError_t configure_predict_t(int sm) {
   return e;
 }
 
+// The limit is the device maximum (shared by all layers; see configure_kernels).
 cudaError_t configure_predict_kernels(const sffn_layer& L) {
-  const int sm = (int)score_smem(L);
+  if (score_smem(L) + 2048 > (size_t)L.smem_optin) return cudaErrorInvalidConfiguration;
+  const int sm = L.smem_optin;
   switch (L.desc.wdtype) {
     case SFFN_F32: return configure_predict_t<float>(sm);
     case SFFN_F16: return configure_predict_t<__half>(sm);

@@ -91,6 +91,7 @@ _sig("sffn_layer_packed", _c, _vp, _P(PackedView))
 _sig("sffn_workspace_bytes", _size, _vp, _i32)
 _sig("sffn_layer_set_trace", _c, _vp, _P(TraceC))
 _sig("sffn_layer_set_next", _c, _vp, _vp)
+_sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
 _sig("sffn_layer_destroy", None, _vp)
 _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
@@ -109,7 +110,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
-    "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next",
+    "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
@@ -216,6 +217,11 @@ def sffn_layer_set_trace(layer, begin=None, end=None) -> None:
 def sffn_layer_set_next(layer, next_layer=None) -> None:
     """L2 hint: ``next_layer`` (a handle, or None) follows ``layer`` on the stream."""
     _check(_lib.sffn_layer_set_next(layer, next_layer), "sffn_layer_set_next")
+
+
+def sffn_layer_set_grid(layer, ffn_blocks: int = 0, score_blocks: int = 0) -> None:
+    """B = 1 grid sizes (0 = one block per SM), for predictor/FFN overlap."""
+    _check(_lib.sffn_layer_set_grid(layer, ffn_blocks, score_blocks), "sffn_layer_set_grid")
 
 
 def sffn_workspace_bytes(layer, B: int) -> int:
@@ -378,6 +384,9 @@ class Layer:
 
     def check_error(self, stream=None) -> None:
         sffn_layer_check_error(self.handle, stream)
+
+    def set_grid(self, ffn_blocks: int = 0, score_blocks: int = 0) -> None:
+        sffn_layer_set_grid(self.handle, ffn_blocks, score_blocks)
 
     def set_next(self, other: "Layer | None") -> None:
         """L2 hint of sffn_layer_set_next; keeps ``other`` alive while set."""

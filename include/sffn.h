@@ -193,6 +193,22 @@ sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* h
  * Errors: INVALID_ARG (layer NULL, or next on another device). */
 sffn_status sffn_layer_set_next(sffn_layer* layer, const sffn_layer* next /* or NULL */);
 
+/* Optional B = 1 grid sizes, for running one layer's predictor and another
+ * layer's sparse FFN at the same time on two streams (one-layer-ahead
+ * prediction: KAIROX observes that adjacent layers see near-identical inputs,
+ * so layer l + 1's active set can be predicted from layer l's input while
+ * layer l's FFN runs). The sparse-FFN kernel holds one large-shared-memory
+ * block per SM and the predictor-scores kernel likewise, so they can only
+ * overlap on disjoint SMs: ffn_blocks limits the FFN kernel and score_blocks
+ * the scores kernel of this layer to that many blocks (0 = one per SM, the
+ * default). The predictor's hidden-layer kernel needs no limit (it shares
+ * SMs). Masks do not depend on the grid; y may differ by fp32 rounding,
+ * because the FFN's per-block partial sums change with the block count.
+ * Host only; the workspace size (sffn_workspace_bytes) never grows.
+ * Errors: INVALID_ARG (layer NULL, a count outside [0, number of SMs], or
+ * too few FFN blocks for the layer's shared-memory ring). */
+sffn_status sffn_layer_set_grid(sffn_layer* layer, int32_t ffn_blocks, int32_t score_blocks);
+
 /* ---------------------------------------------------------------- hot calls */
 
 /* Predictor (PowerInfer §5.1 and the threshold note): for each token b,
