@@ -55,6 +55,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=300)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--lookahead", type=int, default=0, metavar="SMS",
+                   help="B = 1: predict layer l+1 from layer l's input on a second stream while layer l's FFN "
+                        "runs; SMS = SMs given to the predictor (0 = off, the exact method)")
     p.add_argument("--no-prefetch-next", action="store_true",
                    help="do not let each layer prefetch the next layer's predictor weights into L2")
     p.add_argument("--ref-max-steps", type=int, default=24)
@@ -278,6 +281,14 @@ def run_ours(args, world, rank, local):
     if prefetch_next:
         for l in range(nL):
             layers[l].set_next(layers[(l + 1) % nL])
+    # one-layer-ahead prediction: the predictor and the FFN run on disjoint SMs
+    lookahead = args.lookahead if Bt == 1 else 0
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if lookahead:
+        if not 0 < lookahead < n_sms:
+            raise SystemExit(f"--lookahead must lie in 1..{n_sms - 1}")
+        for L in layers:
+            L.set_grid(n_sms - lookahead, lookahead)
 
     # ---- buffers
     P = max(1, min(args.tokens, spec.tokens))
@@ -309,8 +320,40 @@ def run_ours(args, world, rank, local):
     # product + finisher, scores product + finisher, mask views, up/gate
     # product + activation, down product + finisher.
     launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0)
+    if lookahead:
+        launches_per_step += nL   # sffn_predict adds the mask-views kernel
+        pstream = torch.cuda.Stream(device=dev)
+        ws_pred = layers[0].workspace(1, device=dev)
+        ev_x = [torch.cuda.Event() for _ in range(nL)]
+        ev_p = [torch.cuda.Event() for _ in range(nL)]
 
-    def step(t, xin=None):
+    def layers_pass(x, saved=None):
+        """One token through every layer on `stream`; returns the last x_out.
+        Exact method: sffn_decode_step per layer. Look-ahead: layer 0 is
+        predicted from its own input, layer l + 1 from x_l on `pstream` while
+        layer l's FFN runs (sffn_forward). `saved` collects each layer's input."""
+        outb = (xa, xb)
+        if lookahead:
+            sffn.sffn_predict(layers[0].handle, x, 1, spec.thres, masks[0], ws_pred, stream)
+        for l in range(nL):
+            xo = outb[l % 2]
+            if saved is not None:
+                saved.append(x.clone())
+            if not lookahead:
+                sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
+            else:
+                if l + 1 < nL:
+                    ev_x[l].record(stream)
+                    pstream.wait_event(ev_x[l])
+                    sffn.sffn_predict(layers[l + 1].handle, x, 1, spec.thres, masks[l + 1], ws_pred, pstream)
+                    ev_p[l].record(pstream)
+                sffn.sffn_forward(layers[l].handle, x, 1, masks[l], ybuf, xo, ws, stream)
+                if l + 1 < nL:
+                    stream.wait_event(ev_p[l])
+            x = xo
+        return x
+
+    def step(t, xin=None, saved=None):
         """Token t through every layer; in parallel, on a side stream, the
         momentum update (and lambda step) of token t-1, whose group masks sit in
         the other parity buffer. One momentum update per step."""
@@ -322,21 +365,31 @@ def run_ours(args, world, rank, local):
             sffn.tam_adapt(tam.handle, 0, nL, stalls[(t - 1) % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, side)
         ev_join.record(side)
         x = X[t % P] if xin is None else xin
-        outb = (xa, xb)
         for l in range(nL):
             set_tam_mask(l, gmask_buf[par, l].data_ptr())
-            xo = outb[l % 2]
-            sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
-            x = xo
+        x = layers_pass(x, saved)
         stream.wait_event(ev_join)
         return x
 
     # ---- census: active counts per (token, layer); deterministic given the token
     counts = np.zeros((P, nL), dtype=np.int64)       # active (B = 1) or union (B > 1) neurons
     tok_counts = np.zeros((P, nL), dtype=np.int64)   # sum over tokens of their own active neurons
+    la_hits = la_exact = la_extra = 0   # look-ahead vs exact masks along the same trajectory
+    ex_masks = layers[0].masks(1, device=dev) if lookahead else None
+
+    def bits(t_):
+        return int(np.unpackbits(t_.cpu().numpy().view(np.uint8)).sum())
     with torch.cuda.stream(stream):
         for t in range(P):
-            xl = step(t)
+            saved = [] if lookahead else None
+            xl = step(t, saved=saved)
+            if lookahead:
+                for l in range(1, nL):
+                    sffn.sffn_predict(layers[l].handle, saved[l], 1, spec.thres, ex_masks, ws_pred, stream)
+                    la, ex = masks[l].nmask[0], ex_masks.nmask[0]
+                    la_hits += bits(la & ex)
+                    la_exact += bits(ex)
+                    la_extra += bits(la & ~ex)
             if not bool(torch.isfinite(xl).all()):
                 raise SystemExit(f"{spec.name}: the residual stream overflowed within {nL} layers (a gated FFN grows "
                                  "with the square of its input and this stack has no block normalisation); "
@@ -420,15 +473,11 @@ def run_ours(args, world, rank, local):
     tam_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
     with torch.cuda.stream(stream):
         for r in range(R):
-            x = X[r % P]
-            outb = (xa, xb)
             for l in range(nL):
                 sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KN],
                                           [ev[k][r][l][1] for k in KN])
                 set_tam_mask(l, gmask_all[l].data_ptr())
-                xo = outb[l % 2]
-                sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
-                x = xo
+            layers_pass(X[r % P])
             tam_ev[r][0].record(stream)
             sffn.tam_update(tam.handle, 0, nL, gmask_all, gw, -1.0, spec.tam_eps, K, outs, stream)
             tam_ev[r][1].record(stream)
@@ -579,6 +628,12 @@ def run_ours(args, world, rank, local):
     if replicas_note:
         line["config"]["replicas"] = replicas_note
     line["census"] = {"distinct_tokens": P, "active_count_token0_by_layer": [int(c) for c in counts[0]]}
+    if lookahead:
+        line["config"]["mode"] = "one-layer-ahead prediction (layer l+1 predicted from layer l's input)"
+        line["config"]["sm_split"] = {"predictor": lookahead, "ffn": n_sms - lookahead}
+        line["lookahead"] = {"recall": round(la_hits / max(1, la_exact), 4),
+                             "extra_over_exact": round(la_extra / max(1, la_exact), 4),
+                             "note": "layers 1.. of every census token; layer 0 is predicted from its own input"}
     if Bt > 1:
         line["union_frac"] = round(float(counts.mean() / spec.f), 5)
         tpk, _ = measured_tensor_peak()
