@@ -59,10 +59,14 @@ def _check_batch(host, spec, X, thres, masks, y):
 
 
 SHAPES = [
-    # d, f, h, G, act, dtype
+    # d, f, h, G, act, dtype. The down product stages 4, 2 or 1 output tiles of
+    # 128 per K block depending on d / 128 (8, 16 -> 4; 6 -> 2; 3 -> 1); the
+    # contiguous products stage 4 K blocks when h (or d) is a multiple of 256.
     (1024, 2048, 128, 32, "relu", "f16"),
     (1024, 4096, 256, 64, "reglu", "bf16"),
     (2048, 2048, 64, 32, "swiglu", "bf16"),
+    (768, 2048, 192, 64, "reglu", "f16"),
+    (384, 1024, 64, 32, "relu", "bf16"),
 ]
 
 
