@@ -152,7 +152,8 @@ def mask_views(active: np.ndarray, group_size: int) -> dict:
 # Sparse FFN over the active neurons (PowerInfer §5.3-§5.4)
 # --------------------------------------------------------------------------
 
-ACTS = ("relu", "reglu", "swiglu")
+ACTS = ("relu", "reglu", "swiglu", "relu2")
+GATED = ("reglu", "swiglu")   # activations that read a gate row
 
 
 def activation(act: str, u: np.ndarray, g: np.ndarray | None) -> np.ndarray:
@@ -161,11 +162,15 @@ def activation(act: str, u: np.ndarray, g: np.ndarray | None) -> np.ndarray:
     relu:   h = max(0, u)                      (ReLU FFN, no gate)
     reglu:  h = max(0, g) * u                  (ReGLU)
     swiglu: h = g / (1 + exp(-g)) * u          (SiLU-gated, SwiGLU)
+    relu2:  h = max(0, u)^2                    (squared ReLU, no gate)
     PowerInfer names the ReLU family and SiLU-based models (activation note,
-    §4, §8.4); the released code supports ReLU and ReGLU.
+    §4, §8.4); its "Paper vs code" list names ReLU, ReGLU and squared ReLU.
     """
     if act == "relu":
         return np.maximum(u, 0.0)
+    if act == "relu2":
+        r = np.maximum(u, 0.0)
+        return r * r
     if act == "reglu":
         return np.maximum(g, 0.0) * u
     if act == "swiglu":

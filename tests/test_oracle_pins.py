@@ -121,6 +121,7 @@ def test_ffn_swiglu_relu_closed_form(golden):
     one = np.ones_like(g)
     assert np.allclose(O.activation("swiglu", one, g) - O.activation("swiglu", one, -g), g, atol=1e-14)
     assert O.activation("relu", np.array([-2.0, 3.0]), None).tolist() == [0.0, 3.0]
+    assert O.activation("relu2", np.array([-2.0, 3.0, 0.5]), None).tolist() == [0.0, 9.0, 0.25]
     assert O.activation("reglu", np.array([5.0, 5.0]), np.array([-1.0, 2.0])).tolist() == [0.0, 10.0]
 
 
@@ -128,7 +129,7 @@ def test_ffn_swiglu_relu_closed_form(golden):
 
 def _rand_layer(rng, d, f, act):
     up = rng.standard_normal((f, d))
-    gate = rng.standard_normal((f, d)) if act != "relu" else None
+    gate = rng.standard_normal((f, d)) if act in ("reglu", "swiglu") else None
     down = rng.standard_normal((d, f))
     return up, gate, down
 
@@ -138,6 +139,8 @@ def _torch_dense(x, up, gate, down, act):
     u = F.linear(xt, torch.from_numpy(up))
     if act == "relu":
         h = F.relu(u)
+    elif act == "relu2":
+        h = torch.square(F.relu(u))
     elif act == "reglu":
         h = F.relu(F.linear(xt, torch.from_numpy(gate))) * u
     else:
@@ -145,7 +148,7 @@ def _torch_dense(x, up, gate, down, act):
     return F.linear(h, torch.from_numpy(down)).numpy()
 
 
-@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu"])
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
 def test_all_active_equals_library_dense(act):
     rng = np.random.default_rng(7)
     d, f, h = 24, 64, 16
@@ -164,7 +167,7 @@ def test_all_active_equals_library_dense(act):
     assert np.allclose(r["scores"], s[perm], rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu"])
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
 def test_none_active_is_exact_zero(act):
     rng = np.random.default_rng(8)
     d, f, h = 16, 64, 8
@@ -178,7 +181,7 @@ def test_none_active_is_exact_zero(act):
 # ---------------------------------------------------------------- brute force d=8
 
 @pytest.mark.parametrize("f", [32, 64])
-@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu"])
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
 def test_brute_force_masks_d8(f, act):
     """For random masks, y equals the library dense FFN with the inactive
     neurons' up/gate rows and down columns zeroed; disjoint masks add."""
