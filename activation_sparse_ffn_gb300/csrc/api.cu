@@ -114,7 +114,8 @@ sffn_status sffn_layer_validate(const sffn_layer_desc* desc) {
   if (!desc) return invalid("desc is NULL");
   const sffn_layer_desc& D = *desc;
   if (D.wdtype != SFFN_F32 && D.wdtype != SFFN_F16 && D.wdtype != SFFN_BF16) return invalid("wdtype is not an sffn_dtype");
-  if (D.act != SFFN_ACT_RELU && D.act != SFFN_ACT_REGLU && D.act != SFFN_ACT_SWIGLU) return invalid("act is not an sffn_act");
+  if (D.act != SFFN_ACT_RELU && D.act != SFFN_ACT_REGLU && D.act != SFFN_ACT_SWIGLU && D.act != SFFN_ACT_RELU2)
+    return invalid("act is not an sffn_act");
   if (D.d < 8 || D.d > 16384 || D.d % 8) return invalid("d must be a multiple of 8 in [8, 16384]");
   if ((long long)D.d * wbytes_of(D.wdtype) > 32768) return invalid("a weight row (d * element size) must be at most 32 KB");
   if (D.h < 8 || D.h % 8) return invalid("h must be a positive multiple of 8");
@@ -162,7 +163,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
       {&L->W2, f * h * wb},
       {(void**)&L->b2, f * 4},
       {&L->up, f * d * wb},
-      {&L->gate, desc->act == SFFN_ACT_RELU ? 0 : f * d * wb},
+      {&L->gate, act_gated(desc->act) ? f * d * wb : 0},
       {&L->downT, f * d * wb},
       {(void**)&L->perm, f * 4},
       {(void**)&L->err, 256},
@@ -194,13 +195,13 @@ sffn_status sffn_layer_pack(sffn_layer* L, const void* W1, const float* b1, cons
                             sffn_stream stream) {
   if (!L) return invalid("layer is NULL");
   if (!W1 || !W2 || !up || !down) return invalid("W1, W2, up and down are required");
-  if (L->desc.act != SFFN_ACT_RELU && !gate) return invalid("gate is required for ReGLU and SwiGLU");
+  if (act_gated(L->desc.act) && !gate) return invalid("gate is required for ReGLU and SwiGLU");
   const void* ptrs[] = {W1, W2, up, down, gate, b1, b2, perm};
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) return invalid("weight, bias and perm pointers must be 16-byte aligned");
   sffn_status rc = check_device(L->device);
   if (rc != SFFN_OK) return rc;
-  return pack_layer(*L, W1, b1, W2, b2, up, L->desc.act == SFFN_ACT_RELU ? nullptr : gate, down, perm,
+  return pack_layer(*L, W1, b1, W2, b2, up, act_gated(L->desc.act) ? gate : nullptr, down, perm,
                     (cudaStream_t)stream);
 }
 

@@ -559,9 +559,9 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
   if (u >= (U + kTileK - 1) / kTileK * kTileK) return;  // the down product reads no further
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (u < U && nq * 4 < B) {
-    const Plan p = make_plan(false, U, d, grid, ksub_gather(d, ACT != SFFN_ACT_RELU ? 2 : 1));  // the up/gate plan
+    const Plan p = make_plan(false, U, d, grid, ksub_gather(d, act_gated(ACT) ? 2 : 1));  // the up/gate plan
     const float4 au = sum_segments(Du, p, u, npad, nq);
-    const float4 ag = ACT != SFFN_ACT_RELU ? sum_segments(Dg, p, u, npad, nq) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 ag = act_gated(ACT) ? sum_segments(Dg, p, u, npad, nq) : make_float4(0.f, 0.f, 0.f, 0.f);
     const int slot = ld_dep(uidx + u);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -868,7 +868,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   if (e != cudaSuccess || !forward) return e;
 
   // up/gate over the union rows: D[U x N] = {up, gate} . X^T over K = d
-  const bool gated = L.desc.act != SFFN_ACT_RELU;
+  const bool gated = act_gated(L.desc.act);
   const size_t dmat = rows_bound(L, (f + kTileM - 1) / kTileM) * npad;
   GemmArgs u{};
   u.A0 = static_cast<const unsigned char*>(L.up);
@@ -897,6 +897,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   switch (L.desc.act) {
     case SFFN_ACT_RELU: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_RELU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_RELU); break;
     case SFFN_ACT_REGLU: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_REGLU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_REGLU); break;
+    case SFFN_ACT_RELU2: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_RELU2) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_RELU2); break;
     default: e = bf ? SFFN_ACT_LAUNCH(__nv_bfloat16, SFFN_ACT_SWIGLU) : SFFN_ACT_LAUNCH(__half, SFFN_ACT_SWIGLU); break;
   }
 #undef SFFN_ACT_LAUNCH

@@ -219,6 +219,10 @@ __device__ __forceinline__ float relu_nan(float v) { return v < 0.f ? 0.f : v; }
 template <int ACT>
 __device__ __forceinline__ float neuron_act(float u, float g) {
   if (ACT == SFFN_ACT_RELU) return relu_nan(u);
+  if (ACT == SFFN_ACT_RELU2) {
+    const float r = relu_nan(u);
+    return r * r;
+  }
   if (ACT == SFFN_ACT_REGLU) return relu_nan(g) * u;
   return g / (1.f + expf(-g)) * u;  // SiLU(g) * u
 }

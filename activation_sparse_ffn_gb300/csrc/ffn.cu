@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes) {
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
-  constexpr bool GATED = ACT != SFFN_ACT_RELU;
+  constexpr bool GATED = act_gated(ACT);
   constexpr int NMAT = GATED ? 2 : 1;  // rows per ring stage in both phases
   const uint32_t row_bytes = (uint32_t)d * sizeof(T);
   const uint32_t stage_bytes = row_bytes * NMAT;
@@ -347,13 +347,13 @@ cudaError_t set_max_carveout();
 int ffn_blocks(const sffn_layer& L) { return ffn_grid_of(L); }
 
 int ffn_stages_for(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.wbytes * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
+  const size_t stage = (size_t)L.desc.d * L.wbytes * (act_gated(L.desc.act) ? 2 : 1);
   const size_t budget = kFfnSmemBudget > ffn_fixed_smem(L) ? kFfnSmemBudget - ffn_fixed_smem(L) : 0;
   return (int)std::min<size_t>(kFfnMaxStages, budget / (stage + 16));
 }
 
 size_t ffn_smem(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.wbytes * (L.desc.act == SFFN_ACT_RELU ? 1 : 2);
+  const size_t stage = (size_t)L.desc.d * L.wbytes * (act_gated(L.desc.act) ? 2 : 1);
   return (size_t)L.ffn_stages * (stage + 16) + ffn_fixed_smem(L);
 }
 
@@ -365,18 +365,17 @@ cudaError_t configure_kernels(sffn_layer& L) {
   const size_t sm = (size_t)L.smem_optin;
   cudaError_t e = set_max_carveout();
   if (e != cudaSuccess) return e;
+#define SFFN_FFN_ATTRS(T)                                                                                   \
+  if ((e = set_ffn_attr<T, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<T, SFFN_ACT_REGLU>(sm)) ||              \
+      (e = set_ffn_attr<T, SFFN_ACT_SWIGLU>(sm)))                                                            \
+    return e;                                                                                                \
+  return set_ffn_attr<T, SFFN_ACT_RELU2>(sm);
   switch (L.desc.wdtype) {
-    case SFFN_F32:
-      if ((e = set_ffn_attr<float, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<float, SFFN_ACT_REGLU>(sm))) return e;
-      return set_ffn_attr<float, SFFN_ACT_SWIGLU>(sm);
-    case SFFN_F16:
-      if ((e = set_ffn_attr<__half, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<__half, SFFN_ACT_REGLU>(sm))) return e;
-      return set_ffn_attr<__half, SFFN_ACT_SWIGLU>(sm);
-    default:
-      if ((e = set_ffn_attr<__nv_bfloat16, SFFN_ACT_RELU>(sm)) || (e = set_ffn_attr<__nv_bfloat16, SFFN_ACT_REGLU>(sm)))
-        return e;
-      return set_ffn_attr<__nv_bfloat16, SFFN_ACT_SWIGLU>(sm);
+    case SFFN_F32: SFFN_FFN_ATTRS(float)
+    case SFFN_F16: SFFN_FFN_ATTRS(__half)
+    default: SFFN_FFN_ATTRS(__nv_bfloat16)
   }
+#undef SFFN_FFN_ATTRS
 }
 
 
@@ -392,6 +391,9 @@ cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmas
                                             gmask_out, partials);                     \
     case SFFN_ACT_REGLU:                                                                                     \
       return launch_ffn_t<T, SFFN_ACT_REGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
+                                             gmask_out, partials);                    \
+    case SFFN_ACT_RELU2:                                                                                     \
+      return launch_ffn_t<T, SFFN_ACT_RELU2>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
                                              gmask_out, partials);                    \
     default:                                                                                                 \
       return launch_ffn_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,      \

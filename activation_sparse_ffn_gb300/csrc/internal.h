@@ -56,6 +56,9 @@ struct tam_state {
 
 namespace sffn {
 
+// Whether an activation reads a gate row (ReGLU, SwiGLU) or not (ReLU, squared ReLU).
+__host__ __device__ constexpr bool act_gated(int act) { return act == SFFN_ACT_REGLU || act == SFFN_ACT_SWIGLU; }
+
 constexpr int kFfnSmemBudget = 224 * 1024;
 constexpr int kFfnMaxStages = 12;
 constexpr int kScoreSmemBudget = 192 * 1024;

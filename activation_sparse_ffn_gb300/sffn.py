@@ -34,7 +34,7 @@ SFFN_ERR_TIMEOUT = 4
 SFFN_ERR_OOM = 5
 SFFN_ERR_DEVICE = 6
 
-ACT = {"relu": 0, "reglu": 1, "swiglu": 2}
+ACT = {"relu": 0, "reglu": 1, "swiglu": 2, "relu2": 3}
 DTYPE = {"f32": 0, "f16": 1, "bf16": 2}
 TORCH_WDTYPE = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 

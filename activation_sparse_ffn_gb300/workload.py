@@ -54,7 +54,7 @@ class LayerSpec:
     f: int                      # FFN neurons
     h: int                      # predictor hidden size
     group_size: int             # co-activation group size G
-    act: str                    # "relu" | "reglu" | "swiglu"
+    act: str                    # "relu" | "reglu" | "swiglu" | "relu2" (squared ReLU)
     wdtype: str                 # "f32" | "f16" | "bf16"
     p_mean: float               # mean firing probability per token
     zipf_alpha: float | None = None          # fixed alpha, or
@@ -93,7 +93,12 @@ class LayerSpec:
 
     @property
     def n_mats(self) -> int:
-        return 2 if self.act == "relu" else 3
+        return 3 if self.gated else 2
+
+    @property
+    def gated(self) -> bool:
+        """ReGLU and SwiGLU read a gate row per neuron; ReLU and squared ReLU do not."""
+        return self.act in ("reglu", "swiglu")
 
 
 # The workloads, named by what they are.
@@ -302,7 +307,7 @@ def make_layer(spec: LayerSpec, seed: int = 0, layer: int = 0, device="cpu", top
         b2[perm.long()] = b2_slot
     up = _normal((f, d), 1.0 / math.sqrt(d), _gen(device, seed, "up", layer), device).to(dt)
     gate = None
-    if spec.act != "relu":
+    if spec.gated:
         gate = _normal((f, d), 1.0 / math.sqrt(d), _gen(device, seed, "gate", layer), device).to(dt)
     down = None
     if with_down:

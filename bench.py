@@ -190,7 +190,7 @@ def batch_layer_cost(spec, ucount: int, B: int, with_b2: bool) -> dict:
     executed per product (128-row tiles, N padded to 16/32, two MMAs per
     product for the hi/lo parts of the activations)."""
     d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
-    nmat_up = 1 if spec.act == "relu" else 2
+    nmat_up = 2 if spec.gated else 1
     npad = 16 if B <= 16 else 32
     tiles = lambda m: -(-m // 128) * 128
     k = {
@@ -521,7 +521,7 @@ def run_ours(args, world, rank, local):
         for L in layers:
             pv = L.packed()
             mk = lambda ptr: sffn.view_device(ptr, (spec.f, spec.d), tdt)
-            views.append((mk(pv.up), mk(pv.gate) if spec.act != "relu" else None, mk(pv.downT)))
+            views.append((mk(pv.up), mk(pv.gate) if spec.gated else None, mk(pv.downT)))
 
         def dense_lib(l, xv):
             up, gate, downT = views[l]
@@ -529,6 +529,8 @@ def run_ours(args, world, rank, local):
             u = torch.matmul(up, xt)                 # [f][B]
             if spec.act == "relu":
                 hh = torch.relu(u)
+            elif spec.act == "relu2":
+                hh = torch.square(torch.relu(u))
             else:
                 g = torch.matmul(gate, xt)
                 hh = (torch.relu(g) if spec.act == "reglu" else torch.nn.functional.silu(g)) * u

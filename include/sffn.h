@@ -58,7 +58,10 @@ typedef enum {
   SFFN_ERR_DEVICE = 6         /* the device found bad data (e.g. perm not a permutation) */
 } sffn_status;
 
-typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_REGLU = 1, SFFN_ACT_SWIGLU = 2 } sffn_act;
+/* h = ReLU(u) | ReLU(g) * u | SiLU(g) * u | ReLU(u)^2 (squared ReLU, PowerInfer's
+ * "Paper vs code" list), with u = up . x and g = gate . x; only ReGLU and
+ * SwiGLU read gate rows. */
+typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_REGLU = 1, SFFN_ACT_SWIGLU = 2, SFFN_ACT_RELU2 = 3 } sffn_act;
 typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
 
 /* Shape of one FFN layer and its predictor.
@@ -67,7 +70,7 @@ typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
  *   h: predictor hidden size, multiple of 8, h * element size <= 2 KB
  *      (h <= 1024 for 16-bit weights, h <= 512 for fp32).
  *   group_size: 32 or 64 (KAIROX groups).
- *   act: sffn_act. ReLU reads up and down; ReGLU and SwiGLU also read gate.
+ *   act: sffn_act. ReLU and squared ReLU read up and down; ReGLU and SwiGLU also read gate.
  *   wdtype: storage type of every weight matrix (fp32 accumulation always).
  *   max_batch: largest B the layer will be called with, 1..32. */
 typedef struct {
@@ -102,7 +105,7 @@ typedef struct tam_state tam_state;
 /* Device addresses of a layer's packed arrays (read-only view, for tests and
  * tools): W1 [h][d], b1 [h] (fp32, zeros if none), W2 [f][h] in slot order,
  * b2 [f] (fp32, slot order, zeros if none), up/gate/downT [f][d] in slot order
- * (gate NULL for ReLU; downT[s][:] is column perm[s] of down), perm [f]. */
+ * (gate NULL for ReLU and squared ReLU; downT[s][:] is column perm[s] of down), perm [f]. */
 typedef struct {
   const void* W1;
   const float* b1;
@@ -135,7 +138,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out);
 /* Pack row-major weights into the grouped, neuron-major layout (setup, not a
  * hot call; synchronizes the stream before returning):
  *   W1 [h][d], W2 [f][h] (row n = original neuron n), up [f][d],
- *   gate [f][d] (NULL for ReLU, required otherwise), down [d][f] (column n =
+ *   gate [f][d] (NULL for ReLU and squared ReLU, required otherwise), down [d][f] (column n =
  *   original neuron n), all in the layer's wdtype; b1 [h], b2 [f] fp32 or NULL
  *   (zero); perm [f] int32 with perm[slot] = original neuron id, or NULL for
  *   the identity. Slot s of the packed arrays holds neuron perm[s]; down is

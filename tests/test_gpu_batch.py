@@ -67,6 +67,7 @@ SHAPES = [
     (2048, 2048, 64, 32, "swiglu", "bf16"),
     (768, 2048, 192, 64, "reglu", "f16"),
     (384, 1024, 64, 32, "relu", "bf16"),
+    (1024, 2048, 128, 64, "relu2", "f16"),
 ]
 
 

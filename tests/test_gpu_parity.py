@@ -58,6 +58,8 @@ SMALL = [
     (8192, 1024, 1024, 64, "reglu", "bf16"),
     (24, 64, 16, 32, "reglu", "f32"),
     (8, 32, 8, 32, "relu", "bf16"),
+    (1536, 2048, 96, 32, "relu2", "bf16"),
+    (520, 960, 64, 32, "relu2", "f32"),
 ]
 
 
@@ -112,7 +114,7 @@ def test_pack_rejects_non_permutation(sffn):
 
 # ------------------------------------------------------------------ special cases
 
-@pytest.mark.parametrize("act,dt", [("relu", "f32"), ("reglu", "bf16"), ("swiglu", "f16")])
+@pytest.mark.parametrize("act,dt", [("relu", "f32"), ("reglu", "bf16"), ("swiglu", "f16"), ("relu2", "bf16")])
 def test_all_active_and_none_active(sffn, act, dt):
     spec = W.LayerSpec(name="t", d=1024, f=2048, h=128, group_size=32, act=act, wdtype=dt, p_mean=0.1,
                        zipf_alpha=1.0)
