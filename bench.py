@@ -71,6 +71,19 @@ def dist_env():
     return world, rank, local
 
 
+def replica_job_rate(elapsed_ms: float, units_per_rank: float, world: int, device="cpu"):
+    """Replicas only (no collective on the data path): every rank processes its
+    own units; the job's elapsed time is the slowest rank's (max over ranks)
+    and its rate counts the units of all ranks. Returns (elapsed_ms, rate)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms, world * units_per_rank / (elapsed_ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -450,18 +463,13 @@ def run_ours(args, world, rank, local):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms, value = replica_job_rate(ev0.elapsed_time(ev1), Bt * args.steps, world, dev)
     for L in layers:
         L.check_error(stream)
     sffn.tam_check_error(tam.handle, stream)
     toks = [(t_start + i) % P for i in range(args.steps)]
     timed_bytes = float(sum(metric_bytes[t] for t in toks))
     sec = elapsed_ms / 1e3
-    value = world * Bt * args.steps / sec
     ms_per_step = elapsed_ms / args.steps
     step_gbs = timed_bytes / sec / 1e9
 
