@@ -218,6 +218,25 @@ def ffn_sparse_stored(x: np.ndarray, up_s, gate_s, down_s, dtype: str, act: str,
     return ffn_sparse(x, U, G, D, act, np.ones(orig.shape[0], dtype=bool), None)
 
 
+def ffn_sparse_q8(x: np.ndarray, up_q, up_scale, gate_q, gate_scale, down_q, down_scale, act: str,
+                  active: np.ndarray, perm=None) -> tuple[np.ndarray, np.ndarray]:
+    """:func:`ffn_sparse` on 8-bit quantized rows (the quantized models of the
+    pages' Q4/Q8 runs, here one int8 code per weight and one float32 scale per
+    neuron): the weight is code x scale. up_q, gate_q (f, d) int8 with
+    up_scale, gate_scale (f,) float32, one per neuron row; down_q (d, f) int8
+    with down_scale (f,) float32, one per neuron column; original neuron order.
+    Only the active neurons' codes are widened (exactly, to float64)."""
+    f = up_q.shape[0]
+    perm = np.arange(f) if perm is None else np.asarray(perm)
+    orig = perm[np.flatnonzero(active)]
+    U = up_q[orig].astype(np.float64) * up_scale[orig].astype(np.float64)[:, None]
+    G = None
+    if gate_q is not None:
+        G = gate_q[orig].astype(np.float64) * gate_scale[orig].astype(np.float64)[:, None]
+    D = down_q[:, orig].astype(np.float64) * down_scale[orig].astype(np.float64)[None, :]
+    return ffn_sparse(x, U, G, D, act, np.ones(orig.shape[0], dtype=bool), None)
+
+
 # --------------------------------------------------------------------------
 # One layer, one or more tokens
 # --------------------------------------------------------------------------

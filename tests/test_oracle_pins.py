@@ -395,3 +395,46 @@ def test_tam_candidate_is_strict():
                  dtype=np.float32)
     cand, topk = O.tam_select(s, tau, 5)
     assert cand.tolist() == [False, True, False] and topk.tolist() == [1]
+
+
+# ---------------------------------------------------------------- 8-bit quantized rows
+
+def test_q8_hand_computed():
+    """One neuron, d = 4: u = 0.5 * (q_up . x), ReLU, y = h * 0.25 * q_down."""
+    up_q = np.array([[1, -2, 3, 0]], dtype=np.int8)
+    x = np.array([1.0, 2.0, -1.0, 3.0])                        # q . x = 1 - 4 - 3 + 0 = -6
+    x2 = np.array([2.0, 0.0, 1.0, 1.0])                        # q . x2 = 2 + 0 + 3 + 0 = 5
+    down_q = np.array([[2], [0], [-1], [4]], dtype=np.int8)
+    s_up = np.array([0.5], dtype=np.float32)
+    s_dn = np.array([0.25], dtype=np.float32)
+    y, h = O.ffn_sparse_q8(x2, up_q, s_up, None, None, down_q, s_dn, "relu", np.array([True]))
+    assert h.tolist() == [2.5]                                 # 0.5 * 5
+    assert y.tolist() == [1.25, 0.0, -0.625, 2.5]              # 2.5 * 0.25 * [2, 0, -1, 4]
+    y0, _ = O.ffn_sparse_q8(x, up_q, s_up, None, None, down_q, s_dn, "relu", np.array([True]))
+    assert (y0 == 0.0).all()                                   # u = -3 < 0
+
+
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
+def test_q8_all_active_equals_library_dense(act):
+    """Codes times per-neuron scales, dequantized by torch and run through a
+    library dense FFN, equal the oracle's quantized sparse FFN with every
+    neuron active (scales differ per neuron, so a scale applied along the
+    wrong axis fails)."""
+    rng = np.random.default_rng(11)
+    d, f = 24, 64
+    up_q = rng.integers(-127, 128, (f, d)).astype(np.int8)
+    gate_q = rng.integers(-127, 128, (f, d)).astype(np.int8) if act in ("reglu", "swiglu") else None
+    down_q = rng.integers(-127, 128, (d, f)).astype(np.int8)
+    s_up = rng.uniform(1e-3, 2e-2, f).astype(np.float32)
+    s_g = rng.uniform(1e-3, 2e-2, f).astype(np.float32)
+    s_dn = rng.uniform(1e-3, 2e-2, f).astype(np.float32)
+    perm = rng.permutation(f)
+    x = rng.standard_normal(d)
+    y, _ = O.ffn_sparse_q8(x, up_q, s_up, gate_q, s_g if gate_q is not None else None, down_q, s_dn, act,
+                           np.ones(f, dtype=bool), perm)
+    up = torch.from_numpy(up_q).double() * torch.from_numpy(s_up).double()[:, None]
+    gate = (torch.from_numpy(gate_q).double() * torch.from_numpy(s_g).double()[:, None]).numpy() \
+        if gate_q is not None else None
+    down = torch.from_numpy(down_q).double() * torch.from_numpy(s_dn).double()[None, :]
+    ref = _torch_dense(x, up.numpy(), gate, down.numpy(), act)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
