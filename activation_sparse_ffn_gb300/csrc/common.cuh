@@ -195,6 +195,27 @@ struct WType<__nv_bfloat16> {
   }
 };
 
+// 8-bit codes of quantized FFN rows (the row's scale is applied by the caller).
+template <>
+struct WType<int8_t> {
+  static constexpr int kPerChunk = 16;
+  // Exact conversion with full-rate instructions only (an int-to-float
+  // conversion issues at a fraction of the FMA rate): flipping the sign bit
+  // turns code b into the unsigned byte u = b + 128; placing u in the low
+  // byte of the bit pattern 0x4B000000 gives the float 2^23 + u exactly; one
+  // subtraction of 2^23 + 128 leaves b.
+  __device__ __forceinline__ static void unpack(const uint4& v, float* o) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    constexpr float kBias = 8388608.f + 128.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[4 * i + j] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u | j)) - kBias;
+    }
+  }
+};
+
 // Dot product of one 16-byte weight chunk with kPerChunk fp32 values.
 template <typename T>
 __device__ __forceinline__ float dot_chunk(const uint4& w, const float* x) {

@@ -22,12 +22,16 @@
 #include "scan.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace sffn {
 
 namespace {
 
 constexpr int kConsumerWarps = 8;
+
+// Neurons per ring stage of k_ffn for weights of `wbytes` bytes.
+__host__ __device__ constexpr int neurons_per_stage(int wbytes) { return wbytes == 1 ? 4 : 1; }
 constexpr int kFfnThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kReduceThreads = 256;
@@ -50,13 +54,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
     k_ffn(const T* __restrict__ up, const T* __restrict__ gate, const T* __restrict__ downT, const float* x,
           const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages, int list_cap,
           int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, uint32_t* __restrict__ gmask_out,
-          float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes) {
+          float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes,
+          const float* __restrict__ up_s, const float* __restrict__ gate_s, const float* __restrict__ down_s) {
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = act_gated(ACT);
-  constexpr int NMAT = GATED ? 2 : 1;  // rows per ring stage in both phases
+  // 8-bit rows: codes times one scale per neuron (up_s, gate_s, down_s)
+  constexpr bool Q8 = std::is_same<T, int8_t>::value;
+  constexpr int NMAT = GATED ? 2 : 1;  // rows per neuron in phase A
+  // neurons per ring stage: 8-bit rows are half as long, and a stage costs
+  // a roughly fixed time on top of its bytes, so their stages carry 4 neurons
+  constexpr int NPS = neurons_per_stage(sizeof(T));
   const uint32_t row_bytes = (uint32_t)d * sizeof(T);
-  const uint32_t stage_bytes = row_bytes * NMAT;
+  const uint32_t stage_bytes = row_bytes * NMAT * NPS;
   const int nch = (int)(row_bytes / 16);
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -94,8 +104,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   }
   __syncthreads();
 
-  const int nA = n_local;                      // phase A units: one neuron (up [+ gate])
-  const int nB = (n_local + NMAT - 1) / NMAT;  // phase B units: NMAT downT rows
+  const int nA = (n_local + NPS - 1) / NPS;                  // phase A stages: NPS neurons' up [+ gate]
+  const int nB = (n_local + NMAT * NPS - 1) / (NMAT * NPS);  // phase B stages: NMAT * NPS downT rows
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == kConsumerWarps) {
     // ---------------- producer
@@ -113,13 +123,17 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         }
         unsigned char* dst = ring + (size_t)s * stage_bytes;
         if (u < nA) {
-          const size_t slot = (size_t)s_list[u];
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          bulk_g2s(dst, up + slot * d, row_bytes, &full[s], pol);
-          if (GATED) bulk_g2s(dst + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+          const int k0 = u * NPS, nk = min(NPS, n_local - k0);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nk * NMAT * row_bytes);
+          for (int k = 0; k < nk; ++k) {
+            const size_t slot = (size_t)s_list[k0 + k];
+            unsigned char* dk = dst + (size_t)k * NMAT * row_bytes;
+            bulk_g2s(dk, up + slot * d, row_bytes, &full[s], pol);
+            if (GATED) bulk_g2s(dk + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+          }
         } else {
-          const int r0 = (u - nA) * NMAT;
-          const int nr = min(NMAT, n_local - r0);
+          const int r0 = (u - nA) * NMAT * NPS;
+          const int nr = min(NMAT * NPS, n_local - r0);
           mbar_arrive_expect_tx(&full[s], (uint32_t)nr * row_bytes);
           for (int i = 0; i < nr; ++i)
             bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s], pol);
@@ -154,21 +168,26 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           }
           break;
         }
-        const unsigned char* sp = ring + (size_t)s * stage_bytes;
-        float pu = 0.f, pg = 0.f;
+        const int k0 = u * NPS;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c = threadIdx.x + j * kConsumers;
-          if (c < nch) {
-            pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
-            if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+        for (int k = 0; k < NPS; ++k) {
+          if (k0 + k >= n_local) break;
+          const unsigned char* sp = ring + (size_t)s * stage_bytes + (size_t)k * NMAT * row_bytes;
+          float pu = 0.f, pg = 0.f;
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) {
+            const int c = threadIdx.x + j * kConsumers;
+            if (c < nch) {
+              pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
+              if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+            }
           }
-        }
-        pu = warp_sum(pu);
-        if (GATED) pg = warp_sum(pg);
-        if (lane == 0) {
-          s_part[((size_t)u * kConsumerWarps + warp) * 2] = pu;
-          s_part[((size_t)u * kConsumerWarps + warp) * 2 + 1] = pg;
+          pu = warp_sum(pu);
+          if (GATED) pg = warp_sum(pg);
+          if (lane == 0) {
+            s_part[((size_t)(k0 + k) * kConsumerWarps + warp) * 2] = pu;
+            s_part[((size_t)(k0 + k) * kConsumerWarps + warp) * 2 + 1] = pg;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -176,14 +195,22 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
     }
     consumer_barrier();
     // activation of every local neuron, partials added in warp order
-    for (int a = threadIdx.x; a < nA; a += kConsumers) {
+    for (int a = threadIdx.x; a < n_local; a += kConsumers) {
       float uu = 0.f, gg = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
         uu += s_part[((size_t)a * kConsumerWarps + w) * 2];
         gg += s_part[((size_t)a * kConsumerWarps + w) * 2 + 1];
       }
-      s_h[a] = neuron_act<ACT>(uu, gg);
+      if (Q8) {
+        const int slot = s_list[a];
+        uu *= up_s[slot];
+        if (GATED) gg *= gate_s[slot];
+        // phase B multiplies the downT codes by h x the neuron's down scale
+        s_h[a] = neuron_act<ACT>(uu, gg) * down_s[slot];
+      } else {
+        s_h[a] = neuron_act<ACT>(uu, gg);
+      }
       if (idx_out) idx_out[lo + a] = s_list[a];
     }
     consumer_barrier();
@@ -206,8 +233,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           break;
         }
         const unsigned char* sp = ring + (size_t)s * stage_bytes;
-        const int r0 = v * NMAT;
-        const int nr = min(NMAT, n_local - r0);
+        const int r0 = v * NMAT * NPS;
+        const int nr = min(NMAT * NPS, n_local - r0);
         for (int i = 0; i < nr; ++i) {
           const float hv = s_h[r0 + i];
 #pragma unroll
@@ -300,7 +327,7 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
   const size_t pf_bytes = nx ? (size_t)nx->desc.h * nx->desc.d * nx->wbytes : 0;
 #define SFFN_FFN_ARGS                                                                                         \
   grid, dim3(kFfnThreads), smem, st, true, 1, up, gate, downT, x, nmask, L.nwords, L.n_groups,                \
-      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes
+      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes, L.up_s, L.gate_s, L.down_s
   switch (cpt) {
     case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
     case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);
@@ -327,7 +354,7 @@ cudaError_t set_ffn_attr(size_t smem) {
 }
 
 int ffn_cpt(const sffn_layer& L) {
-  const int nch = L.desc.d * L.wbytes / 16;
+  const int nch = L.desc.d * L.fbytes / 16;
   const int need = (nch + kConsumers - 1) / kConsumers;
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
 }
@@ -347,13 +374,13 @@ cudaError_t set_max_carveout();
 int ffn_blocks(const sffn_layer& L) { return ffn_grid_of(L); }
 
 int ffn_stages_for(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.wbytes * (act_gated(L.desc.act) ? 2 : 1);
+  const size_t stage = (size_t)L.desc.d * L.fbytes * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbytes);
   const size_t budget = kFfnSmemBudget > ffn_fixed_smem(L) ? kFfnSmemBudget - ffn_fixed_smem(L) : 0;
   return (int)std::min<size_t>(kFfnMaxStages, budget / (stage + 16));
 }
 
 size_t ffn_smem(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.wbytes * (act_gated(L.desc.act) ? 2 : 1);
+  const size_t stage = (size_t)L.desc.d * L.fbytes * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbytes);
   return (size_t)L.ffn_stages * (stage + 16) + ffn_fixed_smem(L);
 }
 
@@ -370,6 +397,9 @@ cudaError_t configure_kernels(sffn_layer& L) {
       (e = set_ffn_attr<T, SFFN_ACT_SWIGLU>(sm)))                                                            \
     return e;                                                                                                \
   return set_ffn_attr<T, SFFN_ACT_RELU2>(sm);
+  if (L.desc.ffn_format == SFFN_FFN_Q8) {
+    SFFN_FFN_ATTRS(int8_t)
+  }
   switch (L.desc.wdtype) {
     case SFFN_F32: SFFN_FFN_ATTRS(float)
     case SFFN_F16: SFFN_FFN_ATTRS(__half)
@@ -398,6 +428,9 @@ cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmas
     default:                                                                                                 \
       return launch_ffn_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,      \
                                               gmask_out, partials);                   \
+  }
+  if (L.desc.ffn_format == SFFN_FFN_Q8) {
+    SFFN_FFN_DISPATCH(int8_t)
   }
   switch (L.desc.wdtype) {
     case SFFN_F32: SFFN_FFN_DISPATCH(float)

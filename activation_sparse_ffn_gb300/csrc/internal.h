@@ -18,7 +18,8 @@ struct sffn_layer {
   // B = 1 grid sizes (sffn_layer_set_grid); 0 = one block per SM
   int ffn_grid = 0;
   int score_grid = 0;
-  int wbytes = 0;       // bytes per stored weight
+  int wbytes = 0;       // bytes per stored predictor weight (and FFN weight unless quantized)
+  int fbytes = 0;       // bytes per stored FFN weight (1 for SFFN_FFN_Q8)
   int n_groups = 0;
   int nwords = 0;       // f / 32
   int gwords = 0;       // ceil(n_groups / 32)
@@ -30,6 +31,9 @@ struct sffn_layer {
   void* gate = nullptr;
   void* downT = nullptr;
   int32_t* perm = nullptr;
+  float* up_s = nullptr;     // SFFN_FFN_Q8: per-slot row scales
+  float* gate_s = nullptr;
+  float* down_s = nullptr;
   uint32_t* err = nullptr;  // device error word
   bool has_b1 = false, has_b2 = false;
   // launch shapes chosen at create time
@@ -102,9 +106,11 @@ cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8
 cudaError_t launch_selftest_timeout(uint32_t* err, int limit_us, cudaStream_t st);
 
 // Packing (setup).
+// up_s, gate_s, down_s: per-neuron scales of SFFN_FFN_Q8 rows (original order), else null.
 sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const void* W2, const float* b2,
                        const void* up, const void* gate, const void* down, const int32_t* perm,
-                       cudaStream_t st);
+                       cudaStream_t st, const float* up_s = nullptr, const float* gate_s = nullptr,
+                       const float* down_s = nullptr);
 
 // Shared memory sizes, set as kernel attributes at layer creation.
 cudaError_t configure_kernels(sffn_layer& L);

@@ -71,15 +71,21 @@ __global__ void k_transpose(T* __restrict__ dst, const T* __restrict__ src, int 
   }
 }
 
+// Transpose of the FFN's down matrix, moved as raw elements of the layer's
+// FFN element size (4, 2 or 1 bytes).
 cudaError_t transpose(const sffn_layer& L, void* dst, const void* src, int R, int C, cudaStream_t st) {
   const dim3 grid((C + 31) / 32, (R + 31) / 32), block(32, 8);
-  switch (L.desc.wdtype) {
-    case SFFN_F32:
+  switch (L.fbytes) {
+    case 4:
       k_transpose<float><<<grid, block, 0, st>>>(static_cast<float*>(dst), static_cast<const float*>(src), R, C);
       break;
-    default:  // 16-bit types move as raw 16-bit values
+    case 2:
       k_transpose<uint16_t><<<grid, block, 0, st>>>(static_cast<uint16_t*>(dst), static_cast<const uint16_t*>(src),
                                                      R, C);
+      break;
+    default:
+      k_transpose<uint8_t><<<grid, block, 0, st>>>(static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src), R,
+                                                    C);
       break;
   }
   return cudaGetLastError();
@@ -95,9 +101,10 @@ cudaError_t gather_rows(void* dst, const void* src, const int32_t* perm, int row
 }  // namespace
 
 sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const void* W2, const float* b2,
-                       const void* up, const void* gate, const void* down, const int32_t* perm, cudaStream_t st) {
+                       const void* up, const void* gate, const void* down, const int32_t* perm, cudaStream_t st,
+                       const float* up_s, const float* gate_s, const float* down_s) {
   const int d = L.desc.d, f = L.desc.f, h = L.desc.h;
-  const size_t wb = (size_t)L.wbytes;
+  const size_t wb = (size_t)L.wbytes, fb = (size_t)L.fbytes;
   cudaError_t e;
   uint32_t herr = 0;
   void* tmp = nullptr;
@@ -147,11 +154,17 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
     SFFN_TRY(cudaMemsetAsync(L.b2, 0, (size_t)f * 4, st), "pack: b2");
   }
   L.has_b2 = b2 != nullptr;
-  SFFN_TRY(gather_rows(L.up, up, perm, f, (size_t)d * wb, L.err, st), "pack: up");
-  if (L.gate) SFFN_TRY(gather_rows(L.gate, gate, perm, f, (size_t)d * wb, L.err, st), "pack: gate");
-  SFFN_TRY(cudaMalloc(&tmp, (size_t)f * d * wb), "pack: transpose buffer");
+  SFFN_TRY(gather_rows(L.up, up, perm, f, (size_t)d * fb, L.err, st), "pack: up");
+  if (L.gate) SFFN_TRY(gather_rows(L.gate, gate, perm, f, (size_t)d * fb, L.err, st), "pack: gate");
+  SFFN_TRY(cudaMalloc(&tmp, (size_t)f * d * fb), "pack: transpose buffer");
   SFFN_TRY(transpose(L, tmp, down, d, f, st), "pack: transpose down");
-  SFFN_TRY(gather_rows(L.downT, tmp, perm, f, (size_t)d * wb, L.err, st), "pack: downT");
+  SFFN_TRY(gather_rows(L.downT, tmp, perm, f, (size_t)d * fb, L.err, st), "pack: downT");
+  if (L.up_s) {  // quantized rows: each scale follows its neuron into slot order
+    k_gather_f32<<<(f + 255) / 256, 256, 0, st>>>(L.up_s, up_s, perm, f);
+    if (L.gate_s) k_gather_f32<<<(f + 255) / 256, 256, 0, st>>>(L.gate_s, gate_s, perm, f);
+    k_gather_f32<<<(f + 255) / 256, 256, 0, st>>>(L.down_s, down_s, perm, f);
+    SFFN_TRY(cudaGetLastError(), "pack: scales");
+  }
   SFFN_TRY(cudaMemcpyAsync(&herr, L.err, 4, cudaMemcpyDeviceToHost, st), "pack: read error word");
   SFFN_TRY(cudaStreamSynchronize(st), "pack: synchronize");
   if (herr) {

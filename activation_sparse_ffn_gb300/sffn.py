@@ -46,7 +46,7 @@ _i32 = ctypes.c_int32
 
 class LayerDesc(ctypes.Structure):
     _fields_ = [("d", _i32), ("f", _i32), ("h", _i32), ("group_size", _i32), ("act", _i32), ("wdtype", _i32),
-                ("max_batch", _i32)]
+                ("max_batch", _i32), ("ffn_format", _i32)]
 
 
 class MasksC(ctypes.Structure):
@@ -56,7 +56,7 @@ class MasksC(ctypes.Structure):
 
 class PackedView(ctypes.Structure):
     _fields_ = [("W1", _vp), ("b1", _vp), ("W2", _vp), ("b2", _vp), ("up", _vp), ("gate", _vp), ("downT", _vp),
-                ("perm", _vp)]
+                ("perm", _vp), ("up_scale", _vp), ("gate_scale", _vp), ("down_scale", _vp)]
 
 
 class TraceC(ctypes.Structure):
@@ -91,6 +91,7 @@ _sig("sffn_layer_packed", _c, _vp, _P(PackedView))
 _sig("sffn_workspace_bytes", _size, _vp, _i32)
 _sig("sffn_layer_set_trace", _c, _vp, _P(TraceC))
 _sig("sffn_layer_set_next", _c, _vp, _vp)
+_sig("sffn_layer_pack_q8", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
 _sig("sffn_layer_destroy", None, _vp)
@@ -111,6 +112,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
+    "sffn_layer_pack_q8",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
@@ -161,9 +163,13 @@ def version() -> str:
 
 # ----------------------------------------------------------------- layer calls
 
-def make_desc(d, f, h, group_size, act, wdtype, max_batch=1) -> LayerDesc:
+FFN_FORMAT = {"rows": 0, "q8": 1}
+
+
+def make_desc(d, f, h, group_size, act, wdtype, max_batch=1, ffn_format="rows") -> LayerDesc:
     return LayerDesc(d, f, h, group_size, ACT[act] if isinstance(act, str) else act,
-                     DTYPE[wdtype] if isinstance(wdtype, str) else wdtype, max_batch)
+                     DTYPE[wdtype] if isinstance(wdtype, str) else wdtype, max_batch,
+                     FFN_FORMAT[ffn_format] if isinstance(ffn_format, str) else ffn_format)
 
 
 def sffn_layer_validate(desc: LayerDesc) -> int:
@@ -180,6 +186,12 @@ def sffn_layer_create(desc: LayerDesc) -> int:
 def sffn_layer_pack(layer, W1, b1, W2, b2, up, gate, down, perm, stream=None) -> None:
     _check(_lib.sffn_layer_pack(layer, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(up), _ptr(gate), _ptr(down),
                                 _ptr(perm), _stream(stream)), "sffn_layer_pack")
+
+
+def sffn_layer_pack_q8(layer, W1, b1, W2, b2, up_q, up_s, gate_q, gate_s, down_q, down_s, perm, stream=None) -> None:
+    _check(_lib.sffn_layer_pack_q8(layer, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(up_q), _ptr(up_s), _ptr(gate_q),
+                                   _ptr(gate_s), _ptr(down_q), _ptr(down_s), _ptr(perm), _stream(stream)),
+           "sffn_layer_pack_q8")
 
 
 def sffn_layer_get_desc(layer) -> LayerDesc:
@@ -348,20 +360,25 @@ class TamOutputs:
 class Layer:
     """Owns one sffn_layer handle. ``weights`` holds device tensors in the
     original neuron order: W1 (h, d), W2 (f, h), up (f, d), gate (f, d) or
-    None, down (d, f), perm (f,) int32, b1/b2 float32 or None."""
+    None, down (d, f), perm (f,) int32, b1/b2 float32 or None; or, for 8-bit
+    FFN rows, up_q/gate_q (f, d) and down_q (d, f) int8 with up_s/gate_s/down_s
+    (f,) float32 scales in place of up/gate/down."""
 
-    def __init__(self, d, f, h, group_size, act, wdtype, max_batch=1):
-        self.desc = make_desc(d, f, h, group_size, act, wdtype, max_batch)
+    def __init__(self, d, f, h, group_size, act, wdtype, max_batch=1, ffn_format="rows"):
+        self.desc = make_desc(d, f, h, group_size, act, wdtype, max_batch, ffn_format)
+        self.ffn_format = ffn_format
         self.handle = sffn_layer_create(self.desc)
         self.d, self.f, self.h, self.group_size = d, f, h, group_size
         self.act, self.wdtype, self.max_batch = act, wdtype, max_batch
 
     @classmethod
     def from_weights(cls, weights: dict, group_size: int, act: str, max_batch=1, stream=None) -> "Layer":
-        W1, up = weights["W1"], weights["up"]
+        W1 = weights["W1"]
+        q8 = weights.get("up_q") is not None
+        up = weights["up_q"] if q8 else weights["up"]
         h, d = W1.shape
         f = up.shape[0]
-        layer = cls(d, f, h, group_size, act, TORCH_WDTYPE[W1.dtype], max_batch)
+        layer = cls(d, f, h, group_size, act, TORCH_WDTYPE[W1.dtype], max_batch, "q8" if q8 else "rows")
         layer.pack(weights, stream)
         return layer
 
@@ -369,8 +386,14 @@ class Layer:
         def c(t):
             return None if t is None else t.contiguous()
         perm = w.get("perm")
-        sffn_layer_pack(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up"]),
-                        c(w.get("gate")), c(w["down"]), None if perm is None else c(perm.to(torch.int32)), stream)
+        perm = None if perm is None else c(perm.to(torch.int32))
+        if w.get("up_q") is not None:
+            sffn_layer_pack_q8(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up_q"]),
+                               c(w["up_s"]), c(w.get("gate_q")), c(w.get("gate_s")), c(w["down_q"]), c(w["down_s"]),
+                               perm, stream)
+        else:
+            sffn_layer_pack(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up"]),
+                            c(w.get("gate")), c(w["down"]), perm, stream)
 
     def workspace(self, B=1, device="cuda") -> torch.Tensor:
         n = sffn_workspace_bytes(self.handle, B)

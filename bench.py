@@ -226,16 +226,18 @@ def layer_bytes(spec, count: int, with_b2: bool) -> dict:
     """Algorithmic bytes of one layer-token, per kernel: the weight rows the
     method must read plus the small vectors each kernel must move."""
     d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
+    # bytes of one active neuron's FFN rows (plus their scales for 8-bit rows)
+    row = spec.n_mats * (d * spec.fbytes + (4 if spec.ffn_q8 else 0))
     k = {
         "pred_hidden": h * d * wb + d * 4 + h * 4,
         "pred_scores": f * h * wb + h * 4 + f // 8 + (f * 4 if with_b2 else 0),
         # active up/gate/down rows + x + mask words (the per-block partials stay in L2)
-        "ffn": count * spec.n_mats * d * wb + d * 4 + f // 8,
+        "ffn": count * row + d * 4 + f // 8,
         # x read, y and x + y written (partials read from L2 are not HBM traffic)
         "ffn_reduce": 3 * d * 4,
     }
     # the metric: predictor weights + all rows of active neurons + x + y
-    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + count * spec.n_mats * d * wb + 2 * d * 4
+    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + count * row + 2 * d * 4
     return {"kernels": k, "metric": metric}
 
 
@@ -523,7 +525,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     dense_us = 1e3 * e0.elapsed_time(e1) / nd
     dense_lib_us = None
-    if spec.wdtype != "f32":
+    if spec.wdtype != "f32" and not spec.ffn_q8:
         tdt = torch.bfloat16 if spec.wdtype == "bf16" else torch.float16
         views = []
         for L in layers:
@@ -657,6 +659,14 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def oracle_ffn(O, spec, host, x, active, perm):
+    """The oracle's sparse FFN on the stored rows (8-bit codes and scales, or wdtype rows)."""
+    if spec.ffn_q8:
+        return O.ffn_sparse_q8(x, host["up_q"], host["up_s"], host.get("gate_q"), host.get("gate_s"), host["down_q"],
+                               host["down_s"], spec.act, active, perm)
+    return O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, active, perm)
+
+
 def cpu_baseline(spec, host, Xs, seconds):
     """The oracle as it stands on layer 0 of the stack, token after token,
     for about ``seconds``; tokens/s of the whole stack = 1 / (layers x time
@@ -676,7 +686,7 @@ def cpu_baseline(spec, host, Xs, seconds):
         s = O.predictor_scores(W2, O.predictor_hidden(W1, x), host.get("b2f"))[perm]
         a = O.active_from_scores(s, spec.thres)
         O.mask_views(a, spec.group_size)
-        O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, a, perm)
+        oracle_ffn(O, spec, host, x, a, perm)
         times.append(time.perf_counter() - t0)
         t += 1
     per_layer = sum(times) / len(times)
@@ -715,7 +725,7 @@ def run_reference(args, world, rank, local):
         s = O.predictor_scores(W2, O.predictor_hidden(W1, x), b2)[perm]
         a = O.active_from_scores(s, spec.thres)
         O.mask_views(a, spec.group_size)
-        O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, a, perm)
+        oracle_ffn(O, spec, host, x, a, perm)
 
     K = max(1, min(args.steps, args.ref_max_steps))
     Wm = min(args.warmup, 2)

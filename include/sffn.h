@@ -64,6 +64,12 @@ typedef enum {
 typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_REGLU = 1, SFFN_ACT_SWIGLU = 2, SFFN_ACT_RELU2 = 3 } sffn_act;
 typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
 
+/* Storage of the FFN rows (up, gate, down): in the layer's wdtype, or as 8-bit
+ * codes with one fp32 scale per neuron (weight = code x scale; the quantized
+ * models the pages run, here in their 8-bit form). The predictor (W1, W2)
+ * always uses wdtype. */
+typedef enum { SFFN_FFN_ROWS = 0, SFFN_FFN_Q8 = 1 } sffn_ffn_format;
+
 /* Shape of one FFN layer and its predictor.
  *   d: model dimension, multiple of 8, 8 <= d <= 16384.
  *   f: FFN neurons, multiple of group_size, f / group_size <= 1024 groups.
@@ -78,6 +84,8 @@ typedef struct {
   int32_t act;
   int32_t wdtype;
   int32_t max_batch;
+  int32_t ffn_format;   /* sffn_ffn_format; SFFN_FFN_Q8 needs wdtype fp16/bf16 and d % 16 == 0,
+                           and batched calls (B > 1) are not implemented for it */
 } sffn_layer_desc;
 
 /* One token's (or a batch's) active-set views, all device buffers owned by the
@@ -115,6 +123,10 @@ typedef struct {
   const void* gate;
   const void* downT;
   const int32_t* perm;
+  /* SFFN_FFN_Q8 only (NULL otherwise): per-slot scales of up, gate, downT rows */
+  const float* up_scale;
+  const float* gate_scale;
+  const float* down_scale;
 } sffn_packed_view;
 
 /* ---------------------------------------------------------------- status */
@@ -148,6 +160,19 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out);
 sffn_status sffn_layer_pack(sffn_layer* layer, const void* W1, const float* b1, const void* W2,
                             const float* b2, const void* up, const void* gate, const void* down,
                             const int32_t* perm, sffn_stream stream);
+
+/* sffn_layer_pack for an SFFN_FFN_Q8 layer: W1, b1, W2, b2, perm as there;
+ * up_q, gate_q [f][d] int8 codes with up_scale, gate_scale [f] fp32 (one per
+ * neuron row), down_q [d][f] int8 codes with down_scale [f] fp32 (one per
+ * neuron column), all in original neuron order; gate_q and gate_scale NULL
+ * for ReLU and squared ReLU. Packed like sffn_layer_pack (slot order, down
+ * transposed); the scales follow their rows. Device pointers, 16-byte
+ * aligned. Errors: INVALID_ARG (also: the layer is not SFFN_FFN_Q8), DEVICE,
+ * OOM, CUDA. The plain sffn_layer_pack rejects SFFN_FFN_Q8 layers. */
+sffn_status sffn_layer_pack_q8(sffn_layer* layer, const void* W1, const float* b1, const void* W2,
+                               const float* b2, const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
+                               const float* gate_scale, const int8_t* down_q, const float* down_scale,
+                               const int32_t* perm, sffn_stream stream);
 
 sffn_status sffn_layer_get_desc(const sffn_layer* layer, sffn_layer_desc* out /* host */);
 sffn_status sffn_layer_packed(const sffn_layer* layer, sffn_packed_view* out /* host */);

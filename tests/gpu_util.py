@@ -40,9 +40,15 @@ class HostLayer:
         self.dt = wdtype
         self.W1 = O.widen(W.stored_numpy(w["W1"]), wdtype)
         self.W2 = O.widen(W.stored_numpy(w["W2"]), wdtype)
-        self.up = W.stored_numpy(w["up"])
-        self.gate = W.stored_numpy(w["gate"]) if w.get("gate") is not None else None
-        self.down = W.stored_numpy(w["down"])
+        self.q8 = w.get("up_q") is not None     # 8-bit FFN rows: codes and per-neuron scales
+        if self.q8:
+            self.q = {k: (w[k].cpu().numpy() if w.get(k) is not None else None)
+                      for k in ("up_q", "up_s", "gate_q", "gate_s", "down_q", "down_s")}
+            self.up = self.gate = self.down = None
+        else:
+            self.up = W.stored_numpy(w["up"])
+            self.gate = W.stored_numpy(w["gate"]) if w.get("gate") is not None else None
+            self.down = W.stored_numpy(w["down"])
         self.perm = w["perm"].cpu().numpy().astype(np.int64) if w.get("perm") is not None else None
         self.b1 = None if w.get("b1") is None else w["b1"].double().cpu().numpy()
         self.b2 = None if w.get("b2") is None else w["b2"].double().cpu().numpy()
@@ -55,6 +61,11 @@ class HostLayer:
         return s if self.perm is None else s[self.perm]
 
     def ffn(self, x: np.ndarray, active_slots: np.ndarray, act: str) -> np.ndarray:
+        if self.q8:
+            q = self.q
+            y, _ = O.ffn_sparse_q8(x, q["up_q"], q["up_s"], q["gate_q"], q["gate_s"], q["down_q"], q["down_s"], act,
+                                   active_slots, self.perm)
+            return y
         y, _ = O.ffn_sparse_stored(x, self.up, self.gate, self.down, self.dt, act, active_slots, self.perm)
         return y
 

@@ -65,6 +65,12 @@ def test_status_strings(lib):
     (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="f32", max_batch=33), False),
     (dict(d=512, f=2048, h=64, group_size=32, act=7, wdtype="f32"), False),
     (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype=9), False),
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format="q8"), True),
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="f32", ffn_format="q8"), False),   # fp32 predictor
+    (dict(d=520, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format="q8"), False),  # d % 16
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format=5), False),
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu2", wdtype="bf16"), True),
+    (dict(d=512, f=2048, h=64, group_size=32, act=4, wdtype="bf16"), False),
 ])
 def test_validate(lib, kw, ok):
     desc = lib.make_desc(**kw)

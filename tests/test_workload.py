@@ -120,9 +120,10 @@ def test_perm_is_permutation_and_stored_dtypes():
             spec = W.spec_replace(spec, union_target=(32, 0.6))
         L = W.make_layer(spec, seed=0, layer=0)
         assert sorted(L["perm"].tolist()) == list(range(spec.f))
-        assert L["W1"].dtype == W.torch_dtype(spec.wdtype) and L["up"].shape == (spec.f, spec.d)
-        assert L["down"].shape == (spec.d, spec.f)
-        assert (L["gate"] is None) == (spec.act == "relu")
+        sfx = "_q" if spec.ffn_q8 else ""
+        assert L["W1"].dtype == W.torch_dtype(spec.wdtype) and L["up" + sfx].shape == (spec.f, spec.d)
+        assert L["down" + sfx].shape == (spec.d, spec.f)
+        assert (L["gate" + sfx] is None) == (not spec.gated)
 
 
 def test_stall_bits():
@@ -130,3 +131,26 @@ def test_stall_bits():
     assert s.shape == (1024, 32) and s.dtype == np.uint8
     assert abs(s.mean() - 0.5) < 0.02
     assert (s == W.make_stall_bits(1024, 32, seed=0)).all()
+
+
+def test_quantize_rows_q8():
+    g = torch.Generator().manual_seed(0)
+    w = torch.randn(64, 48, generator=g).to(torch.bfloat16)
+    w[3] = 0.0
+    q, s = W.quantize_rows_q8(w)
+    assert q.dtype == torch.int8 and s.dtype == torch.float32 and q.shape == w.shape and s.shape == (64,)
+    assert int(q.abs().max()) <= 127
+    nz = torch.arange(64) != 3
+    assert (q[nz].abs().amax(dim=1) == 127).all()          # the largest |w| of a row maps to 127
+    assert s[3] == 1.0 and (q[3] == 0).all()
+    err = (q.float() * s[:, None] - w.float()).abs()
+    assert (err <= s[:, None] / 2 + 1e-7).all()            # rounding to the nearest code
+
+
+def test_q8_layer_fields():
+    spec = W.spec_replace(W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q8_8l"], d=256, f=512, h=64)
+    w = W.make_layer(spec, seed=0)
+    assert w["up"] is None and w["gate"] is None and w["down"] is None
+    assert w["up_q"].shape == (512, 256) and w["gate_q"].shape == (512, 256) and w["down_q"].shape == (256, 512)
+    assert w["up_s"].shape == w["gate_s"].shape == w["down_s"].shape == (512,)
+    assert W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q8_8l"].fbytes == 1
