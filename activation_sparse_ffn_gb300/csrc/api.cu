@@ -280,6 +280,13 @@ sffn_status sffn_layer_set_grid(sffn_layer* L, int32_t ffn_blocks, int32_t score
   return SFFN_OK;
 }
 
+sffn_status sffn_layer_set_l2_resident(sffn_layer* L, const uint32_t* resident) {
+  if (!L) return invalid("layer is NULL");
+  if (resident && (reinterpret_cast<uintptr_t>(resident) & 3)) return invalid("resident must be 4-byte aligned");
+  L->l2_resident = resident;
+  return SFFN_OK;
+}
+
 sffn_status sffn_layer_set_next(sffn_layer* L, const sffn_layer* next) {
   if (!L) return invalid("layer is NULL");
   if (next && next->device != L->device) return invalid("sffn_layer_set_next: next lives on another device");

@@ -91,6 +91,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// Lines read under this policy are the last to leave L2.
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // One-dimensional bulk copy global -> this CTA's shared memory; completion is
 // signalled on `bar` as transaction bytes. dst, src and bytes must be
 // multiples of 16.

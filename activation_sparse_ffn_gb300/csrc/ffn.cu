@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           const uint32_t* nmask, int nw, int n_groups, int G, int gwords, int d, int stages, int list_cap,
           int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, uint32_t* __restrict__ gmask_out,
           float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes,
-          const float* __restrict__ up_s, const float* __restrict__ gate_s, const float* __restrict__ down_s) {
+          const float* __restrict__ up_s, const float* __restrict__ gate_s, const float* __restrict__ down_s,
+          const uint32_t* resident) {
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = act_gated(ACT);
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   float* s_part = s_h + list_cap;  // [list_cap][warps][2]
   __shared__ int s_tmp[NT / 32];
   __shared__ int s_abort;
+  __shared__ uint32_t s_res[32];  // L2-resident groups (at most 1024)
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -98,6 +100,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   const int hi = (int)((long long)total * (b + 1) / nb);
   const int n_local = min(hi - lo, list_cap);
   extract_slice<NT>(s_words, s_off, nw, lo, lo + n_local, s_list);
+  // the optional hot-group set (may be written by the previous kernel)
+  if (threadIdx.x < 32) s_res[threadIdx.x] = (resident && (int)threadIdx.x < gwords) ? ld_dep(resident + threadIdx.x) : 0u;
   if (b == 0) {
     if (threadIdx.x == 0 && count_out) *count_out = total;
     if (gmask_out) write_group_mask<NT>(s_words, n_groups, G, gwords, gmask_out);
@@ -110,7 +114,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   if (warp == kConsumerWarps) {
     // ---------------- producer
     if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
+      // rows of hot groups stay in L2 for the next tokens, the rest streams through
+      const uint64_t pol_stream = l2_policy_evict_first(), pol_keep = l2_policy_keep();
+      auto pol_of = [&](int slot) {
+        const int g = slot / G;
+        return (s_res[g >> 5] >> (g & 31)) & 1u ? pol_keep : pol_stream;
+      };
       for (int u = 0; u < nA + nB; ++u) {
         const int s = u % stages;
         const bool ok = u < stages || mbar_wait_bounded(&empty[s], (uint32_t)((u / stages - 1) & 1));
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           mbar_arrive_expect_tx(&full[s], (uint32_t)nk * NMAT * row_bytes);
           for (int k = 0; k < nk; ++k) {
             const size_t slot = (size_t)s_list[k0 + k];
+            const uint64_t pol = pol_of((int)slot);
             unsigned char* dk = dst + (size_t)k * NMAT * row_bytes;
             bulk_g2s(dk, up + slot * d, row_bytes, &full[s], pol);
             if (GATED) bulk_g2s(dk + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
@@ -136,7 +146,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           const int nr = min(NMAT * NPS, n_local - r0);
           mbar_arrive_expect_tx(&full[s], (uint32_t)nr * row_bytes);
           for (int i = 0; i < nr; ++i)
-            bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s], pol);
+            bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s],
+                     pol_of(s_list[r0 + i]));
         }
       }
       // L2 hint: once this block's rows are all requested, its share of the
@@ -327,7 +338,8 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
   const size_t pf_bytes = nx ? (size_t)nx->desc.h * nx->desc.d * nx->wbytes : 0;
 #define SFFN_FFN_ARGS                                                                                         \
   grid, dim3(kFfnThreads), smem, st, true, 1, up, gate, downT, x, nmask, L.nwords, L.n_groups,                \
-      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes, L.up_s, L.gate_s, L.down_s
+      L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes, L.up_s, L.gate_s, L.down_s, \
+      L.l2_resident
   switch (cpt) {
     case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
     case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);

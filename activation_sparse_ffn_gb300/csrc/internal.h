@@ -42,6 +42,8 @@ struct sffn_layer {
   // optional L2 hint (sffn_layer_set_next): the layer whose predictor weights
   // this layer's FFN kernel prefetches
   const sffn_layer* next = nullptr;
+  // optional hot-group set (sffn_layer_set_l2_resident): device bitset [gwords]
+  const uint32_t* l2_resident = nullptr;
   // optional timing hooks (sffn_layer_set_trace)
   cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};

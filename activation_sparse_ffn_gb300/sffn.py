@@ -93,6 +93,7 @@ _sig("sffn_layer_set_trace", _c, _vp, _P(TraceC))
 _sig("sffn_layer_set_next", _c, _vp, _vp)
 _sig("sffn_layer_pack_q8", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
+_sig("sffn_layer_set_l2_resident", _c, _vp, _vp)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
 _sig("sffn_layer_destroy", None, _vp)
 _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
@@ -112,6 +113,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
+    "sffn_layer_set_l2_resident",
     "sffn_layer_pack_q8",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
@@ -234,6 +236,11 @@ def sffn_layer_set_next(layer, next_layer=None) -> None:
 def sffn_layer_set_grid(layer, ffn_blocks: int = 0, score_blocks: int = 0) -> None:
     """B = 1 grid sizes (0 = one block per SM), for predictor/FFN overlap."""
     _check(_lib.sffn_layer_set_grid(layer, ffn_blocks, score_blocks), "sffn_layer_set_grid")
+
+
+def sffn_layer_set_l2_resident(layer, resident=None) -> None:
+    """Hot-group bitset (device uint32 [ceil(n_groups/32)], or None) whose rows stay in L2."""
+    _check(_lib.sffn_layer_set_l2_resident(layer, _ptr(resident)), "sffn_layer_set_l2_resident")
 
 
 def sffn_workspace_bytes(layer, B: int) -> int:
@@ -410,6 +417,11 @@ class Layer:
 
     def set_grid(self, ffn_blocks: int = 0, score_blocks: int = 0) -> None:
         sffn_layer_set_grid(self.handle, ffn_blocks, score_blocks)
+
+    def set_l2_resident(self, resident) -> None:
+        """Hot-group bitset (device tensor or pointer) of sffn_layer_set_l2_resident; keeps a tensor alive."""
+        sffn_layer_set_l2_resident(self.handle, resident)
+        self._resident = resident
 
     def set_next(self, other: "Layer | None") -> None:
         """L2 hint of sffn_layer_set_next; keeps ``other`` alive while set."""

@@ -58,6 +58,9 @@ def parse_args():
     p.add_argument("--lookahead", type=int, default=0, metavar="SMS",
                    help="B = 1: predict layer l+1 from layer l's input on a second stream while layer l's FFN "
                         "runs; SMS = SMs given to the predictor (0 = off, the exact method)")
+    p.add_argument("--l2-resident-mb", type=float, default=0.0, metavar="MB",
+                   help="B = 1: L2 share (all layers) for the rows of hot neuron groups, which a second momentum "
+                        "state sized to that share picks each token; 0 = off")
     p.add_argument("--no-prefetch-next", action="store_true",
                    help="do not let each layer prefetch the next layer's predictor weights into L2")
     p.add_argument("--ref-max-steps", type=int, default=24)
@@ -330,11 +333,21 @@ def run_ours(args, world, rank, local):
     tam = sffn.Tam(nL, spec.n_groups, spec.tam_lambda)
     K = spec.capacity
     outs = sffn.TamOutputs(nL, spec.n_groups, K, device=dev)
+    # optional L2 residency of hot groups: a momentum state whose capacity is
+    # the number of groups per layer that fit the requested L2 share
+    l2_groups = 0
+    if Bt == 1 and args.l2_resident_mb > 0:
+        group_bytes = spec.group_size * spec.n_mats * (spec.d * spec.fbytes + (4 if spec.ffn_q8 else 0))
+        l2_groups = max(1, min(spec.n_groups, int(args.l2_resident_mb * 1e6 / (nL * group_bytes))))
+        tam_l2 = sffn.Tam(nL, spec.n_groups, spec.tam_lambda)
+        outs_l2 = sffn.TamOutputs(nL, spec.n_groups, l2_groups, device=dev)
+        for l in range(nL):
+            layers[l].set_l2_resident(outs_l2.resident[l])
     stalls = torch.from_numpy(W.make_stall_bits(P, nL, seed=args.seed)).to(dev) if spec.anb else None
     # B = 1: hidden, scores, fused FFN, reduction. B > 1: split of x, hidden
     # product + finisher, scores product + finisher, mask views, up/gate
     # product + activation, down product + finisher.
-    launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0)
+    launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0) + (1 if l2_groups else 0)
     if lookahead:
         launches_per_step += nL   # sffn_predict adds the mask-views kernel
         pstream = torch.cuda.Stream(device=dev)
@@ -376,6 +389,8 @@ def run_ours(args, world, rank, local):
         ev_fork.record(stream)
         side.wait_event(ev_fork)
         sffn.tam_update(tam.handle, 0, nL, gmask_buf[1 - par], gw, -1.0, spec.tam_eps, K, outs, side)
+        if l2_groups:
+            sffn.tam_update(tam_l2.handle, 0, nL, gmask_buf[1 - par], gw, -1.0, spec.tam_eps, l2_groups, outs_l2, side)
         if spec.anb:
             sffn.tam_adapt(tam.handle, 0, nL, stalls[(t - 1) % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, side)
         ev_join.record(side)
@@ -615,6 +630,7 @@ def run_ours(args, world, rank, local):
             "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype, "thres": spec.thres,
             "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
             "distinct_tokens": P, "graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
+            "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
             "l2": "inputs larger than L2: each step reads %.2f GB of distinct weights" % (timed_bytes / args.steps / 1e9),
             "parallelism": "replicas" if world > 1 else "single",
         },

@@ -221,6 +221,21 @@ sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* h
  * Errors: INVALID_ARG (layer NULL, or next on another device). */
 sffn_status sffn_layer_set_next(sffn_layer* layer, const sffn_layer* next /* or NULL */);
 
+/* Optional hot-group residency in L2 (the single-GPU analogue of PowerInfer's
+ * hot/cold neuron split, §3-§4, with L2 in place of the GPU and HBM in place of
+ * the CPU; KAIROX's momentum picks the hot groups, 核心方法 item 4). resident is
+ * a device bitset of the layer's groups, [ceil(n_groups / 32)] uint32 (for
+ * instance one layer's row of tam_outputs.resident from tam_update with a
+ * capacity sized to the L2 share it may hold), or NULL to turn the hint off.
+ * The B = 1 sparse-FFN kernel reads it at every launch (so tam_update may
+ * rewrite it on the same stream between calls) and reads the up/gate/downT
+ * rows of predicted-active neurons in those groups with the L2 evict-last
+ * priority, all other rows with evict-first, so that hot rows tend to be
+ * served from L2 on the next tokens. Results are unchanged (cache priorities
+ * only). The caller keeps the buffer alive while it is set. Host only.
+ * Errors: INVALID_ARG (layer NULL, resident not 4-byte aligned). */
+sffn_status sffn_layer_set_l2_resident(sffn_layer* layer, const uint32_t* resident /* device, or NULL */);
+
 /* Optional B = 1 grid sizes, for running one layer's predictor and another
  * layer's sparse FFN at the same time on two streams (one-layer-ahead
  * prediction: KAIROX observes that adjacent layers see near-identical inputs,

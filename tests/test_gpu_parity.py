@@ -204,6 +204,13 @@ def test_l2_hint_leaves_results_unchanged(sffn):
         assert torch.equal(y0, y1) and torch.equal(xo0, xo1)
         for k in ("nmask", "gmask", "idx", "count"):
             assert torch.equal(getattr(m0, k), getattr(m1, k)), k
+    # hot groups read with the L2 keep priority: also unchanged
+    n_gw = (spec.f // spec.group_size + 31) // 32
+    res = torch.randint(0, 2**31, (n_gw,), dtype=torch.int32, device="cuda")
+    A.set_l2_resident(res)
+    m1, y1, xo1 = _decode(sffn, A, x, 0.0, x_out=True)
+    assert torch.equal(y0, y1) and torch.equal(xo0, xo1) and torch.equal(m0.idx, m1.idx)
+    A.set_l2_resident(None)
     A.set_next(Bl)
     y2 = torch.empty(1, spec.d, device="cuda")
     m2 = A.masks()
