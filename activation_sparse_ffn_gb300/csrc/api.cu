@@ -124,9 +124,12 @@ sffn_status sffn_layer_validate(const sffn_layer_desc* desc) {
   if (D.f < D.group_size || D.f % D.group_size) return invalid("f must be a positive multiple of group_size");
   if (D.f / D.group_size > 1024) return invalid("at most 1024 groups per layer");
   if (D.max_batch < 1 || D.max_batch > 32) return invalid("max_batch must be in [1, 32]");
-  if (D.ffn_format != SFFN_FFN_ROWS && D.ffn_format != SFFN_FFN_Q8) return invalid("ffn_format is not an sffn_ffn_format");
+  if (D.ffn_format != SFFN_FFN_ROWS && D.ffn_format != SFFN_FFN_Q8 && D.ffn_format != SFFN_FFN_Q4)
+    return invalid("ffn_format is not an sffn_ffn_format");
   if (D.ffn_format == SFFN_FFN_Q8 && (D.wdtype == SFFN_F32 || D.d % 16))
     return invalid("8-bit FFN rows need a 16-bit predictor (wdtype fp16 or bf16) and d a multiple of 16");
+  if (D.ffn_format == SFFN_FFN_Q4 && (D.wdtype == SFFN_F32 || D.d % 32))
+    return invalid("4-bit FFN rows need a 16-bit predictor (wdtype fp16 or bf16) and d a multiple of 32");
   return SFFN_OK;
 }
 
@@ -138,7 +141,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   if (!L) return invalid("host allocation failed");
   L->desc = *desc;
   L->wbytes = wbytes_of(desc->wdtype);
-  L->fbytes = desc->ffn_format == SFFN_FFN_Q8 ? 1 : L->wbytes;
+  L->fbits = desc->ffn_format == SFFN_FFN_Q8 ? 8 : desc->ffn_format == SFFN_FFN_Q4 ? 4 : 8 * L->wbytes;
   L->n_groups = desc->f / desc->group_size;
   L->nwords = desc->f / 32;
   L->gwords = (L->n_groups + 31) / 32;
@@ -157,8 +160,8 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
     set_error("sffn_layer_create: the FFN ring does not fit in shared memory for this shape");
     return SFFN_ERR_UNSUPPORTED;
   }
-  const size_t d = desc->d, f = desc->f, h = desc->h, wb = L->wbytes, fb = L->fbytes;
-  const bool q8 = desc->ffn_format == SFFN_FFN_Q8;
+  const size_t d = desc->d, f = desc->f, h = desc->h, wb = L->wbytes, frow = ffn_row_bytes(*L);
+  const bool q8 = desc->ffn_format != SFFN_FFN_ROWS;  // scaled codes (8-bit or 4-bit)
   struct {
     void** p;
     size_t bytes;
@@ -167,9 +170,9 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
       {(void**)&L->b1, h * 4},
       {&L->W2, f * h * wb},
       {(void**)&L->b2, f * 4},
-      {&L->up, f * d * fb},
-      {&L->gate, act_gated(desc->act) ? f * d * fb : 0},
-      {&L->downT, f * d * fb},
+      {&L->up, f * frow},
+      {&L->gate, act_gated(desc->act) ? f * frow : 0},
+      {&L->downT, f * frow},
       {(void**)&L->up_s, q8 ? f * 4 : 0},
       {(void**)&L->gate_s, q8 && act_gated(desc->act) ? f * 4 : 0},
       {(void**)&L->down_s, q8 ? f * 4 : 0},
@@ -203,6 +206,7 @@ sffn_status sffn_layer_pack(sffn_layer* L, const void* W1, const float* b1, cons
                             sffn_stream stream) {
   if (!L) return invalid("layer is NULL");
   if (L->desc.ffn_format == SFFN_FFN_Q8) return invalid("this layer stores 8-bit FFN rows: use sffn_layer_pack_q8");
+  if (L->desc.ffn_format == SFFN_FFN_Q4) return invalid("this layer stores 4-bit FFN rows: use sffn_layer_pack_q4");
   if (!W1 || !W2 || !up || !down) return invalid("W1, W2, up and down are required");
   if (act_gated(L->desc.act) && !gate) return invalid("gate is required for ReGLU and SwiGLU");
   const void* ptrs[] = {W1, W2, up, down, gate, b1, b2, perm};
@@ -214,12 +218,11 @@ sffn_status sffn_layer_pack(sffn_layer* L, const void* W1, const float* b1, cons
                     (cudaStream_t)stream);
 }
 
-sffn_status sffn_layer_pack_q8(sffn_layer* L, const void* W1, const float* b1, const void* W2, const float* b2,
-                               const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
-                               const float* gate_scale, const int8_t* down_q, const float* down_scale,
-                               const int32_t* perm, sffn_stream stream) {
-  if (!L) return invalid("layer is NULL");
-  if (L->desc.ffn_format != SFFN_FFN_Q8) return invalid("sffn_layer_pack_q8 needs a layer with ffn_format SFFN_FFN_Q8");
+namespace {
+
+sffn_status pack_codes(sffn_layer* L, const void* W1, const float* b1, const void* W2, const float* b2,
+                       const int8_t* up_q, const float* up_scale, const int8_t* gate_q, const float* gate_scale,
+                       const int8_t* down_q, const float* down_scale, const int32_t* perm, sffn_stream stream) {
   if (!W1 || !W2 || !up_q || !up_scale || !down_q || !down_scale)
     return invalid("W1, W2, up_q, up_scale, down_q and down_scale are required");
   const bool gated = act_gated(L->desc.act);
@@ -231,6 +234,26 @@ sffn_status sffn_layer_pack_q8(sffn_layer* L, const void* W1, const float* b1, c
   if (rc != SFFN_OK) return rc;
   return pack_layer(*L, W1, b1, W2, b2, up_q, gated ? gate_q : nullptr, down_q, perm, (cudaStream_t)stream,
                     up_scale, gated ? gate_scale : nullptr, down_scale);
+}
+
+}  // namespace
+
+sffn_status sffn_layer_pack_q8(sffn_layer* L, const void* W1, const float* b1, const void* W2, const float* b2,
+                               const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
+                               const float* gate_scale, const int8_t* down_q, const float* down_scale,
+                               const int32_t* perm, sffn_stream stream) {
+  if (!L) return invalid("layer is NULL");
+  if (L->desc.ffn_format != SFFN_FFN_Q8) return invalid("sffn_layer_pack_q8 needs a layer with ffn_format SFFN_FFN_Q8");
+  return pack_codes(L, W1, b1, W2, b2, up_q, up_scale, gate_q, gate_scale, down_q, down_scale, perm, stream);
+}
+
+sffn_status sffn_layer_pack_q4(sffn_layer* L, const void* W1, const float* b1, const void* W2, const float* b2,
+                               const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
+                               const float* gate_scale, const int8_t* down_q, const float* down_scale,
+                               const int32_t* perm, sffn_stream stream) {
+  if (!L) return invalid("layer is NULL");
+  if (L->desc.ffn_format != SFFN_FFN_Q4) return invalid("sffn_layer_pack_q4 needs a layer with ffn_format SFFN_FFN_Q4");
+  return pack_codes(L, W1, b1, W2, b2, up_q, up_scale, gate_q, gate_scale, down_q, down_scale, perm, stream);
 }
 
 sffn_status sffn_layer_get_desc(const sffn_layer* L, sffn_layer_desc* out) {

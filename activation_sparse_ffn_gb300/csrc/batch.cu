@@ -753,8 +753,8 @@ BatchWs batch_ws_layout(const sffn_layer& L, int B) {
 }
 
 bool batch_supported(const sffn_layer& L, std::string* why) {
-  if (L.desc.ffn_format == SFFN_FFN_Q8) {
-    if (why) *why = "batched calls need 16-bit FFN rows (8-bit rows run at B = 1)";
+  if (L.desc.ffn_format != SFFN_FFN_ROWS) {
+    if (why) *why = "batched calls need 16-bit FFN rows (8-bit and 4-bit rows run at B = 1)";
     return false;
   }
   if (L.desc.wdtype == SFFN_F32) {

@@ -221,6 +221,62 @@ struct WType<int8_t> {
         o[4 * i + j] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u | j)) - kBias;
     }
   }
+  // The same as pairs (elements 2p, 2p+1), the bias removed two at a time.
+  __device__ __forceinline__ static void unpack2(const uint4& v, float2* o) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    const float2 nb = make_float2(-(8388608.f + 128.f), -(8388608.f + 128.f));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < 4; j += 2)
+        o[2 * i + j / 2] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u | j)),
+                                                  __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7441u | j))),
+                                      nb);
+    }
+  }
+};
+
+// Two signed 4-bit codes in one byte: element 2i in the low half of byte i,
+// element 2i + 1 in the high half (the row's scale is applied by the caller).
+struct q4x2_t {
+  uint8_t v;
+};
+
+template <>
+struct WType<q4x2_t> {
+  static constexpr int kPerChunk = 32;
+  // The 8-bit trick on half-bytes: masking out the low (or high, shifted
+  // down) halves of a word leaves four 4-bit two's-complement codes c, one
+  // per byte; flipping bit 3 turns each into c + 8 in [0, 15]; that byte in
+  // the low byte of 0x4B000000 is the float 2^23 + c + 8, exact; subtracting
+  // 2^23 + 8 leaves c.
+  __device__ __forceinline__ static void unpack(const uint4& v, float* o) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    constexpr float kBias = 8388608.f + 8.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (w[i] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o[8 * i + 2 * j] = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u | j)) - kBias;
+        o[8 * i + 2 * j + 1] = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u | j)) - kBias;
+      }
+    }
+  }
+  // The same as pairs (elements 2p, 2p+1): a pair is the two halves of one byte.
+  __device__ __forceinline__ static void unpack2(const uint4& v, float2* o) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float2 nb = make_float2(-(8388608.f + 8.f), -(8388608.f + 8.f));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (w[i] & 0x0F0F0F0Fu) ^ 0x08080808u, hi = ((w[i] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[4 * i + j] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u | j)),
+                                              __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u | j))),
+                                  nb);
+    }
+  }
 };
 
 // Dot product of one 16-byte weight chunk with kPerChunk fp32 values.
@@ -232,6 +288,22 @@ __device__ __forceinline__ float dot_chunk(const uint4& w, const float* x) {
 #pragma unroll
   for (int i = 0; i < WType<T>::kPerChunk; ++i) s = fmaf(v[i], x[i], s);
   return s;
+}
+
+// Dot product of one 16-byte chunk of codes with kPerChunk fp32 values held
+// as pairs, in packed fp32 arithmetic with two independent accumulators.
+template <typename T>
+__device__ __forceinline__ float dot_chunk_pairs(const uint4& w, const float2* x) {
+  constexpr int NP = WType<T>::kPerChunk / 2;
+  float2 v[NP];
+  WType<T>::unpack2(w, v);
+  float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int p = 0; p < NP; p += 2) {
+    a = __ffma2_rn(v[p], x[p], a);
+    b = __ffma2_rn(v[p + 1], x[p + 1], b);
+  }
+  return (a.x + a.y) + (b.x + b.y);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

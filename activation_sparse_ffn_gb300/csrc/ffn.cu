@@ -30,8 +30,10 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 
-// Neurons per ring stage of k_ffn for weights of `wbytes` bytes.
-__host__ __device__ constexpr int neurons_per_stage(int wbytes) { return wbytes == 1 ? 4 : 1; }
+// Neurons per ring stage for FFN weights of `bits` bits: a stage costs a
+// roughly fixed time on top of its bytes, so the short rows of the quantized
+// formats travel several neurons to a stage.
+__host__ __device__ constexpr int neurons_per_stage(int bits) { return bits == 8 ? 4 : bits == 4 ? 8 : 1; }
 constexpr int kFfnThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kReduceThreads = 256;
@@ -60,13 +62,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = act_gated(ACT);
-  // 8-bit rows: codes times one scale per neuron (up_s, gate_s, down_s)
-  constexpr bool Q8 = std::is_same<T, int8_t>::value;
+  // 8-bit and 4-bit rows: codes times one scale per neuron (up_s, gate_s, down_s)
+  constexpr bool QS = std::is_same<T, int8_t>::value || std::is_same<T, q4x2_t>::value;
   constexpr int NMAT = GATED ? 2 : 1;  // rows per neuron in phase A
-  // neurons per ring stage: 8-bit rows are half as long, and a stage costs
-  // a roughly fixed time on top of its bytes, so their stages carry 4 neurons
-  constexpr int NPS = neurons_per_stage(sizeof(T));
-  const uint32_t row_bytes = (uint32_t)d * sizeof(T);
+  constexpr int NPS = neurons_per_stage(128 / EPC);  // a 16-byte chunk holds EPC weights
+  const uint32_t row_bytes = (uint32_t)(d / EPC) * 16u;
   const uint32_t stage_bytes = row_bytes * NMAT * NPS;
   const int nch = (int)(row_bytes / 16);
 
@@ -138,16 +138,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
             const size_t slot = (size_t)s_list[k0 + k];
             const uint64_t pol = pol_of((int)slot);
             unsigned char* dk = dst + (size_t)k * NMAT * row_bytes;
-            bulk_g2s(dk, up + slot * d, row_bytes, &full[s], pol);
-            if (GATED) bulk_g2s(dk + row_bytes, gate + slot * d, row_bytes, &full[s], pol);
+            bulk_g2s(dk, reinterpret_cast<const unsigned char*>(up) + slot * row_bytes, row_bytes, &full[s], pol);
+            if (GATED)
+              bulk_g2s(dk + row_bytes, reinterpret_cast<const unsigned char*>(gate) + slot * row_bytes, row_bytes,
+                       &full[s], pol);
           }
         } else {
           const int r0 = (u - nA) * NMAT * NPS;
           const int nr = min(NMAT * NPS, n_local - r0);
           mbar_arrive_expect_tx(&full[s], (uint32_t)nr * row_bytes);
           for (int i = 0; i < nr; ++i)
-            bulk_g2s(dst + (size_t)i * row_bytes, downT + (size_t)s_list[r0 + i] * d, row_bytes, &full[s],
-                     pol_of(s_list[r0 + i]));
+            bulk_g2s(dst + (size_t)i * row_bytes,
+                     reinterpret_cast<const unsigned char*>(downT) + (size_t)s_list[r0 + i] * row_bytes, row_bytes,
+                     &full[s], pol_of(s_list[r0 + i]));
         }
       }
       // L2 hint: once this block's rows are all requested, its share of the
@@ -156,8 +159,11 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
     }
   } else {
     // ---------------- consumers, phase A: partial dot products of up/gate rows
+    // (coded rows hold x as pairs for packed fp32 arithmetic: their dequantization
+    // makes them issue-bound, not bandwidth-bound)
     {
-      float xr[CPT][EPC];
+      float xr[CPT][QS ? 1 : EPC];
+      float2 xp[CPT][QS ? EPC / 2 : 1];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
         const int c = threadIdx.x + j * kConsumers;
@@ -165,7 +171,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         for (int e = 0; e < EPC; e += 4) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
           if (c < nch) v = ld_dep4(x + (size_t)c * EPC + e);
-          xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
+          if constexpr (QS) {
+            xp[j][e / 2] = make_float2(v.x, v.y);
+            xp[j][e / 2 + 1] = make_float2(v.z, v.w);
+          } else {
+            xr[j][e] = v.x; xr[j][e + 1] = v.y; xr[j][e + 2] = v.z; xr[j][e + 3] = v.w;
+          }
         }
       }
       for (int u = 0; u < nA; ++u) {
@@ -189,8 +200,14 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           for (int j = 0; j < CPT; ++j) {
             const int c = threadIdx.x + j * kConsumers;
             if (c < nch) {
-              pu += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)c * 16), xr[j]);
-              if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+              const uint4 wu = *reinterpret_cast<const uint4*>(sp + (size_t)c * 16);
+              if constexpr (QS) {
+                pu += dot_chunk_pairs<T>(wu, xp[j]);
+                if (GATED) pg += dot_chunk_pairs<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xp[j]);
+              } else {
+                pu += dot_chunk<T>(wu, xr[j]);
+                if (GATED) pg += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + row_bytes + (size_t)c * 16), xr[j]);
+              }
             }
           }
           pu = warp_sum(pu);
@@ -213,7 +230,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         uu += s_part[((size_t)a * kConsumerWarps + w) * 2];
         gg += s_part[((size_t)a * kConsumerWarps + w) * 2 + 1];
       }
-      if (Q8) {
+      if (QS) {
         const int slot = s_list[a];
         uu *= up_s[slot];
         if (GATED) gg *= gate_s[slot];
@@ -226,11 +243,15 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
     }
     consumer_barrier();
     // ---------------- phase B: acc += h_i * downT_i over this block's neurons
-    float acc[CPT][EPC];
+    float acc[CPT][QS ? 1 : EPC];
+    float2 accp[CPT][QS ? EPC / 2 : 1];  // coded rows: pairs
 #pragma unroll
-    for (int j = 0; j < CPT; ++j)
+    for (int j = 0; j < CPT; ++j) {
 #pragma unroll
-      for (int e = 0; e < EPC; ++e) acc[j][e] = 0.f;
+      for (int e = 0; e < (QS ? 1 : EPC); ++e) acc[j][e] = 0.f;
+#pragma unroll
+      for (int e = 0; e < (QS ? EPC / 2 : 1); ++e) accp[j][e] = make_float2(0.f, 0.f);
+    }
     if (!__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
       for (int v = 0; v < nB; ++v) {
         const int u = nA + v;
@@ -252,10 +273,19 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           for (int j = 0; j < CPT; ++j) {
             const int c = threadIdx.x + j * kConsumers;
             if (c < nch) {
-              float w[EPC];
-              WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)i * row_bytes + (size_t)c * 16), w);
+              const uint4 wv = *reinterpret_cast<const uint4*>(sp + (size_t)i * row_bytes + (size_t)c * 16);
+              if constexpr (QS) {
+                float2 w[EPC / 2];
+                WType<T>::unpack2(wv, w);
+                const float2 h2 = make_float2(hv, hv);
 #pragma unroll
-              for (int e = 0; e < EPC; ++e) acc[j][e] = fmaf(hv, w[e], acc[j][e]);
+                for (int e = 0; e < EPC / 2; ++e) accp[j][e] = __ffma2_rn(h2, w[e], accp[j][e]);
+              } else {
+                float w[EPC];
+                WType<T>::unpack(wv, w);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[j][e] = fmaf(hv, w[e], acc[j][e]);
+              }
             }
           }
         }
@@ -270,9 +300,14 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       const int c = threadIdx.x + j * kConsumers;
       if (c < nch) {
 #pragma unroll
-        for (int e = 0; e < EPC; e += 4)
-          *reinterpret_cast<float4*>(part + (size_t)c * EPC + e) =
-              make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+        for (int e = 0; e < EPC; e += 4) {
+          if constexpr (QS)
+            *reinterpret_cast<float4*>(part + (size_t)c * EPC + e) =
+                make_float4(accp[j][e / 2].x, accp[j][e / 2].y, accp[j][e / 2 + 1].x, accp[j][e / 2 + 1].y);
+          else
+            *reinterpret_cast<float4*>(part + (size_t)c * EPC + e) =
+                make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+        }
       }
     }
   }
@@ -366,7 +401,7 @@ cudaError_t set_ffn_attr(size_t smem) {
 }
 
 int ffn_cpt(const sffn_layer& L) {
-  const int nch = L.desc.d * L.fbytes / 16;
+  const int nch = (int)(ffn_row_bytes(L) / 16);
   const int need = (nch + kConsumers - 1) / kConsumers;
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
 }
@@ -386,13 +421,13 @@ cudaError_t set_max_carveout();
 int ffn_blocks(const sffn_layer& L) { return ffn_grid_of(L); }
 
 int ffn_stages_for(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.fbytes * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbytes);
+  const size_t stage = ffn_row_bytes(L) * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbits);
   const size_t budget = kFfnSmemBudget > ffn_fixed_smem(L) ? kFfnSmemBudget - ffn_fixed_smem(L) : 0;
   return (int)std::min<size_t>(kFfnMaxStages, budget / (stage + 16));
 }
 
 size_t ffn_smem(const sffn_layer& L) {
-  const size_t stage = (size_t)L.desc.d * L.fbytes * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbytes);
+  const size_t stage = ffn_row_bytes(L) * (act_gated(L.desc.act) ? 2 : 1) * neurons_per_stage(L.fbits);
   return (size_t)L.ffn_stages * (stage + 16) + ffn_fixed_smem(L);
 }
 
@@ -409,6 +444,9 @@ cudaError_t configure_kernels(sffn_layer& L) {
       (e = set_ffn_attr<T, SFFN_ACT_SWIGLU>(sm)))                                                            \
     return e;                                                                                                \
   return set_ffn_attr<T, SFFN_ACT_RELU2>(sm);
+  if (L.desc.ffn_format == SFFN_FFN_Q4) {
+    SFFN_FFN_ATTRS(q4x2_t)
+  }
   if (L.desc.ffn_format == SFFN_FFN_Q8) {
     SFFN_FFN_ATTRS(int8_t)
   }
@@ -440,6 +478,9 @@ cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmas
     default:                                                                                                 \
       return launch_ffn_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,      \
                                               gmask_out, partials);                   \
+  }
+  if (L.desc.ffn_format == SFFN_FFN_Q4) {
+    SFFN_FFN_DISPATCH(q4x2_t)
   }
   if (L.desc.ffn_format == SFFN_FFN_Q8) {
     SFFN_FFN_DISPATCH(int8_t)

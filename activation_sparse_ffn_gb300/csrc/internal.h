@@ -19,7 +19,7 @@ struct sffn_layer {
   int ffn_grid = 0;
   int score_grid = 0;
   int wbytes = 0;       // bytes per stored predictor weight (and FFN weight unless quantized)
-  int fbytes = 0;       // bytes per stored FFN weight (1 for SFFN_FFN_Q8)
+  int fbits = 0;        // bits per stored FFN weight (8 for SFFN_FFN_Q8, 4 for SFFN_FFN_Q4)
   int n_groups = 0;
   int nwords = 0;       // f / 32
   int gwords = 0;       // ceil(n_groups / 32)
@@ -31,7 +31,7 @@ struct sffn_layer {
   void* gate = nullptr;
   void* downT = nullptr;
   int32_t* perm = nullptr;
-  float* up_s = nullptr;     // SFFN_FFN_Q8: per-slot row scales
+  float* up_s = nullptr;     // SFFN_FFN_Q8 / Q4: per-slot row scales
   float* gate_s = nullptr;
   float* down_s = nullptr;
   uint32_t* err = nullptr;  // device error word
@@ -61,6 +61,9 @@ struct tam_state {
 };
 
 namespace sffn {
+
+// Bytes of one stored FFN row (d weights).
+inline size_t ffn_row_bytes(const sffn_layer& L) { return (size_t)L.desc.d * L.fbits / 8; }
 
 // Whether an activation reads a gate row (ReGLU, SwiGLU) or not (ReLU, squared ReLU).
 __host__ __device__ constexpr bool act_gated(int act) { return act == SFFN_ACT_REGLU || act == SFFN_ACT_SWIGLU; }
@@ -108,7 +111,7 @@ cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8
 cudaError_t launch_selftest_timeout(uint32_t* err, int limit_us, cudaStream_t st);
 
 // Packing (setup).
-// up_s, gate_s, down_s: per-neuron scales of SFFN_FFN_Q8 rows (original order), else null.
+// up_s, gate_s, down_s: per-neuron scales of SFFN_FFN_Q8 / Q4 rows (original order), else null.
 sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const void* W2, const float* b2,
                        const void* up, const void* gate, const void* down, const int32_t* perm,
                        cudaStream_t st, const float* up_s = nullptr, const float* gate_s = nullptr,

@@ -41,6 +41,26 @@ __global__ void k_gather_rows(unsigned char* __restrict__ dst, const unsigned ch
   for (size_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dp[i] = sp[i];
 }
 
+// dst row s = the 4-bit packing of int8 code row perm[s] of src [rows][d]
+// (identity when perm is null): byte i = (code 2i & 15) | (code 2i+1 & 15) << 4.
+// A code outside [-8, 7] or an out-of-range perm value flags SFFN_ERR_DEVICE.
+__global__ void k_pack_q4_rows(uint8_t* __restrict__ dst, const int8_t* __restrict__ src,
+                               const int32_t* __restrict__ perm, int rows, int d, uint32_t* __restrict__ err) {
+  const int s = blockIdx.x;
+  const int n = perm ? perm[s] : s;
+  if (n < 0 || n >= rows) {
+    if (threadIdx.x == 0) set_device_error(err, SFFN_ERR_DEVICE);
+    return;
+  }
+  const int8_t* sp = src + (size_t)n * d;
+  uint8_t* dp = dst + (size_t)s * (d / 2);
+  for (int i = threadIdx.x; i < d / 2; i += blockDim.x) {
+    const int c0 = sp[2 * i], c1 = sp[2 * i + 1];
+    if (c0 < -8 || c0 > 7 || c1 < -8 || c1 > 7) set_device_error(err, SFFN_ERR_DEVICE);
+    dp[i] = (uint8_t)((c0 & 15) | ((c1 & 15) << 4));
+  }
+}
+
 __global__ void k_gather_f32(float* __restrict__ dst, const float* __restrict__ src, const int32_t* __restrict__ perm,
                              int n) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
@@ -71,11 +91,12 @@ __global__ void k_transpose(T* __restrict__ dst, const T* __restrict__ src, int 
   }
 }
 
-// Transpose of the FFN's down matrix, moved as raw elements of the layer's
-// FFN element size (4, 2 or 1 bytes).
+// Transpose of the FFN's down matrix as given to the pack call, moved as raw
+// elements: 4 or 2 bytes for plain rows, 1 byte for 8-bit and 4-bit codes
+// (which arrive one int8 per code).
 cudaError_t transpose(const sffn_layer& L, void* dst, const void* src, int R, int C, cudaStream_t st) {
   const dim3 grid((C + 31) / 32, (R + 31) / 32), block(32, 8);
-  switch (L.fbytes) {
+  switch (L.fbits >= 8 ? L.fbits / 8 : 1) {
     case 4:
       k_transpose<float><<<grid, block, 0, st>>>(static_cast<float*>(dst), static_cast<const float*>(src), R, C);
       break;
@@ -104,7 +125,9 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
                        const void* up, const void* gate, const void* down, const int32_t* perm, cudaStream_t st,
                        const float* up_s, const float* gate_s, const float* down_s) {
   const int d = L.desc.d, f = L.desc.f, h = L.desc.h;
-  const size_t wb = (size_t)L.wbytes, fb = (size_t)L.fbytes;
+  const size_t wb = (size_t)L.wbytes, frow = ffn_row_bytes(L);
+  const bool q4 = L.fbits == 4;
+  const size_t in_elem = q4 ? 1 : (size_t)L.fbits / 8;  // bytes per element of the caller's up/gate/down
   cudaError_t e;
   uint32_t herr = 0;
   void* tmp = nullptr;
@@ -154,11 +177,21 @@ sffn_status pack_layer(sffn_layer& L, const void* W1, const float* b1, const voi
     SFFN_TRY(cudaMemsetAsync(L.b2, 0, (size_t)f * 4, st), "pack: b2");
   }
   L.has_b2 = b2 != nullptr;
-  SFFN_TRY(gather_rows(L.up, up, perm, f, (size_t)d * fb, L.err, st), "pack: up");
-  if (L.gate) SFFN_TRY(gather_rows(L.gate, gate, perm, f, (size_t)d * fb, L.err, st), "pack: gate");
-  SFFN_TRY(cudaMalloc(&tmp, (size_t)f * d * fb), "pack: transpose buffer");
+  SFFN_TRY(cudaMalloc(&tmp, (size_t)f * d * in_elem), "pack: transpose buffer");
   SFFN_TRY(transpose(L, tmp, down, d, f, st), "pack: transpose down");
-  SFFN_TRY(gather_rows(L.downT, tmp, perm, f, (size_t)d * fb, L.err, st), "pack: downT");
+  if (q4) {  // codes arrive one per int8 and are stored two per byte
+    k_pack_q4_rows<<<f, 256, 0, st>>>(static_cast<uint8_t*>(L.up), static_cast<const int8_t*>(up), perm, f, d, L.err);
+    if (L.gate)
+      k_pack_q4_rows<<<f, 256, 0, st>>>(static_cast<uint8_t*>(L.gate), static_cast<const int8_t*>(gate), perm, f, d,
+                                        L.err);
+    k_pack_q4_rows<<<f, 256, 0, st>>>(static_cast<uint8_t*>(L.downT), static_cast<const int8_t*>(tmp), perm, f, d,
+                                      L.err);
+    SFFN_TRY(cudaGetLastError(), "pack: 4-bit rows");
+  } else {
+    SFFN_TRY(gather_rows(L.up, up, perm, f, frow, L.err, st), "pack: up");
+    if (L.gate) SFFN_TRY(gather_rows(L.gate, gate, perm, f, frow, L.err, st), "pack: gate");
+    SFFN_TRY(gather_rows(L.downT, tmp, perm, f, frow, L.err, st), "pack: downT");
+  }
   if (L.up_s) {  // quantized rows: each scale follows its neuron into slot order
     k_gather_f32<<<(f + 255) / 256, 256, 0, st>>>(L.up_s, up_s, perm, f);
     if (L.gate_s) k_gather_f32<<<(f + 255) / 256, 256, 0, st>>>(L.gate_s, gate_s, perm, f);

@@ -92,6 +92,7 @@ _sig("sffn_workspace_bytes", _size, _vp, _i32)
 _sig("sffn_layer_set_trace", _c, _vp, _P(TraceC))
 _sig("sffn_layer_set_next", _c, _vp, _vp)
 _sig("sffn_layer_pack_q8", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("sffn_layer_pack_q4", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
 _sig("sffn_layer_set_l2_resident", _c, _vp, _vp)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
@@ -114,7 +115,7 @@ EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
     "sffn_layer_set_l2_resident",
-    "sffn_layer_pack_q8",
+    "sffn_layer_pack_q8", "sffn_layer_pack_q4",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
@@ -165,7 +166,7 @@ def version() -> str:
 
 # ----------------------------------------------------------------- layer calls
 
-FFN_FORMAT = {"rows": 0, "q8": 1}
+FFN_FORMAT = {"rows": 0, "q8": 1, "q4": 2}
 
 
 def make_desc(d, f, h, group_size, act, wdtype, max_batch=1, ffn_format="rows") -> LayerDesc:
@@ -194,6 +195,13 @@ def sffn_layer_pack_q8(layer, W1, b1, W2, b2, up_q, up_s, gate_q, gate_s, down_q
     _check(_lib.sffn_layer_pack_q8(layer, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(up_q), _ptr(up_s), _ptr(gate_q),
                                    _ptr(gate_s), _ptr(down_q), _ptr(down_s), _ptr(perm), _stream(stream)),
            "sffn_layer_pack_q8")
+
+
+def sffn_layer_pack_q4(layer, W1, b1, W2, b2, up_q, up_s, gate_q, gate_s, down_q, down_s, perm, stream=None) -> None:
+    """As sffn_layer_pack_q8, with int8 codes in [-8, 7] (packed two per byte by the library)."""
+    _check(_lib.sffn_layer_pack_q4(layer, _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(up_q), _ptr(up_s), _ptr(gate_q),
+                                   _ptr(gate_s), _ptr(down_q), _ptr(down_s), _ptr(perm), _stream(stream)),
+           "sffn_layer_pack_q4")
 
 
 def sffn_layer_get_desc(layer) -> LayerDesc:
@@ -385,7 +393,8 @@ class Layer:
         up = weights["up_q"] if q8 else weights["up"]
         h, d = W1.shape
         f = up.shape[0]
-        layer = cls(d, f, h, group_size, act, TORCH_WDTYPE[W1.dtype], max_batch, "q8" if q8 else "rows")
+        fmt = ("q4" if weights.get("qbits") == 4 else "q8") if q8 else "rows"
+        layer = cls(d, f, h, group_size, act, TORCH_WDTYPE[W1.dtype], max_batch, fmt)
         layer.pack(weights, stream)
         return layer
 
@@ -395,9 +404,9 @@ class Layer:
         perm = w.get("perm")
         perm = None if perm is None else c(perm.to(torch.int32))
         if w.get("up_q") is not None:
-            sffn_layer_pack_q8(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up_q"]),
-                               c(w["up_s"]), c(w.get("gate_q")), c(w.get("gate_s")), c(w["down_q"]), c(w["down_s"]),
-                               perm, stream)
+            pack = sffn_layer_pack_q4 if w.get("qbits") == 4 else sffn_layer_pack_q8
+            pack(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up_q"]), c(w["up_s"]),
+                 c(w.get("gate_q")), c(w.get("gate_s")), c(w["down_q"]), c(w["down_s"]), perm, stream)
         else:
             sffn_layer_pack(self.handle, c(w["W1"]), c(w.get("b1")), c(w["W2"]), c(w.get("b2")), c(w["up"]),
                             c(w.get("gate")), c(w["down"]), perm, stream)

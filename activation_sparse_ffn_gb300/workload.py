@@ -79,6 +79,7 @@ class LayerSpec:
     anb_hi: float = 0.99
     topic_shift_at: int | None = None
     ffn_q8: bool = False        # FFN rows as 8-bit codes with one scale per neuron (predictor stays wdtype)
+    ffn_q4: bool = False        # the same with 4-bit codes (two per stored byte)
 
     @property
     def n_groups(self) -> int:
@@ -93,9 +94,14 @@ class LayerSpec:
         return {"f32": 4, "f16": 2, "bf16": 2}[self.wdtype]
 
     @property
-    def fbytes(self) -> int:
-        """Bytes per stored FFN weight."""
-        return 1 if self.ffn_q8 else self.wbytes
+    def fbytes(self) -> float:
+        """Bytes per stored FFN weight (0.5 for 4-bit codes)."""
+        return 0.5 if self.ffn_q4 else 1 if self.ffn_q8 else self.wbytes
+
+    @property
+    def ffn_quant(self) -> bool:
+        """FFN rows stored as codes with one scale per neuron (8-bit or 4-bit)."""
+        return self.ffn_q8 or self.ffn_q4
 
     @property
     def n_mats(self) -> int:
@@ -128,6 +134,11 @@ WORKLOADS = {
         name="llama2_70b_reglu_d8192_f28672_q8_8l", d=8192, f=28672, h=1024, group_size=64,
         act="reglu", wdtype="bf16", p_mean=0.10, coverage=(0.26, 0.80), layers=8, tokens=512,
         seq="ar1", tam_capacity=224, ffn_q8=True),
+    # ... and with 4-bit FFN rows (PowerInfer runs OPT-30B at Q4).
+    "llama2_70b_reglu_d8192_f28672_q4_8l": LayerSpec(
+        name="llama2_70b_reglu_d8192_f28672_q4_8l", d=8192, f=28672, h=1024, group_size=64,
+        act="reglu", wdtype="bf16", p_mean=0.10, coverage=(0.26, 0.80), layers=8, tokens=512,
+        seq="ar1", tam_capacity=224, ffn_q4=True),
     # Falcon-40B-shaped ReLU layer under batching, fp16, ~7% per token, union ~40% at B=32.
     "falcon40b_relu_d8192_f32768_fp16_batch": LayerSpec(
         name="falcon40b_relu_d8192_f32768_fp16_batch", d=8192, f=32768, h=1024, group_size=32,
@@ -327,6 +338,8 @@ def make_layer(spec: LayerSpec, seed: int = 0, layer: int = 0, device="cpu", top
         "W1": W1s, "W2": W2.to(dt), "b1": None, "b2": b2, "up": up, "gate": gate, "down": down,
         "perm": perm, "p_slot": p_slot,
     }
+    if spec.ffn_q4:
+        return quantize_layer_q8(w, bits=4)
     return quantize_layer_q8(w) if spec.ffn_q8 else w
 
 
@@ -380,25 +393,28 @@ def make_stall_bits(T: int, L: int, seed: int = 0) -> np.ndarray:
 # Host views of stored tensors (for the oracle)
 # --------------------------------------------------------------------------
 
-def quantize_rows_q8(w: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """Symmetric 8-bit codes with one float32 scale per row: scale = max|w| / 127
-    (1 for an all-zero row), code = round(w / scale), which lies in [-127, 127]."""
+def quantize_rows_q8(w: torch.Tensor, bits: int = 8) -> tuple[torch.Tensor, torch.Tensor]:
+    """Symmetric codes with one float32 scale per row: with m = 2^(bits-1) - 1
+    (127 for 8 bits, 7 for 4 bits), scale = max|w| / m (1 for an all-zero
+    row), code = round(w / scale), which lies in [-m, m]; int8 either way."""
+    m = float(2 ** (bits - 1) - 1)
     wf = w.float()
     amax = wf.abs().amax(dim=1)
-    scale = torch.where(amax > 0, amax / 127.0, torch.ones_like(amax))
-    q = torch.clamp(torch.round(wf / scale[:, None]), -127, 127).to(torch.int8)
+    scale = torch.where(amax > 0, amax / m, torch.ones_like(amax))
+    q = torch.clamp(torch.round(wf / scale[:, None]), -m, m).to(torch.int8)
     return q.contiguous(), scale.contiguous()
 
 
-def quantize_layer_q8(w: dict) -> dict:
-    """The layer's FFN rows as 8-bit codes: up and gate one scale per neuron row,
-    down one scale per neuron column. Returns a new dict with up_q/up_s,
-    gate_q/gate_s, down_q/down_s and up/gate/down set to None."""
+def quantize_layer_q8(w: dict, bits: int = 8) -> dict:
+    """The layer's FFN rows as 8-bit (or 4-bit) codes: up and gate one scale per
+    neuron row, down one scale per neuron column. Returns a new dict with
+    up_q/up_s, gate_q/gate_s, down_q/down_s, qbits, and up/gate/down set to None."""
     out = dict(w)
-    out["up_q"], out["up_s"] = quantize_rows_q8(w["up"])
-    out["gate_q"], out["gate_s"] = quantize_rows_q8(w["gate"]) if w.get("gate") is not None else (None, None)
+    out["qbits"] = bits
+    out["up_q"], out["up_s"] = quantize_rows_q8(w["up"], bits)
+    out["gate_q"], out["gate_s"] = quantize_rows_q8(w["gate"], bits) if w.get("gate") is not None else (None, None)
     if w.get("down") is not None:
-        qt, s = quantize_rows_q8(w["down"].t())
+        qt, s = quantize_rows_q8(w["down"].t(), bits)
         out["down_q"], out["down_s"] = qt.t().contiguous(), s
     out["up"] = out["gate"] = out["down"] = None
     return out

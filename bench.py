@@ -230,7 +230,7 @@ def layer_bytes(spec, count: int, with_b2: bool) -> dict:
     method must read plus the small vectors each kernel must move."""
     d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
     # bytes of one active neuron's FFN rows (plus their scales for 8-bit rows)
-    row = spec.n_mats * (d * spec.fbytes + (4 if spec.ffn_q8 else 0))
+    row = spec.n_mats * (int(d * spec.fbytes) + (4 if spec.ffn_quant else 0))
     k = {
         "pred_hidden": h * d * wb + d * 4 + h * 4,
         "pred_scores": f * h * wb + h * 4 + f // 8 + (f * 4 if with_b2 else 0),
@@ -337,7 +337,7 @@ def run_ours(args, world, rank, local):
     # the number of groups per layer that fit the requested L2 share
     l2_groups = 0
     if Bt == 1 and args.l2_resident_mb > 0:
-        group_bytes = spec.group_size * spec.n_mats * (spec.d * spec.fbytes + (4 if spec.ffn_q8 else 0))
+        group_bytes = spec.group_size * spec.n_mats * (int(spec.d * spec.fbytes) + (4 if spec.ffn_quant else 0))
         l2_groups = max(1, min(spec.n_groups, int(args.l2_resident_mb * 1e6 / (nL * group_bytes))))
         tam_l2 = sffn.Tam(nL, spec.n_groups, spec.tam_lambda)
         outs_l2 = sffn.TamOutputs(nL, spec.n_groups, l2_groups, device=dev)
@@ -540,7 +540,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     dense_us = 1e3 * e0.elapsed_time(e1) / nd
     dense_lib_us = None
-    if spec.wdtype != "f32" and not spec.ffn_q8:
+    if spec.wdtype != "f32" and not spec.ffn_quant:
         tdt = torch.bfloat16 if spec.wdtype == "bf16" else torch.float16
         views = []
         for L in layers:
@@ -676,10 +676,11 @@ def run_ours(args, world, rank, local):
 
 
 def oracle_ffn(O, spec, host, x, active, perm):
-    """The oracle's sparse FFN on the stored rows (8-bit codes and scales, or wdtype rows)."""
-    if spec.ffn_q8:
-        return O.ffn_sparse_q8(x, host["up_q"], host["up_s"], host.get("gate_q"), host.get("gate_s"), host["down_q"],
-                               host["down_s"], spec.act, active, perm)
+    """The oracle's sparse FFN on the stored rows (8-bit or 4-bit codes and scales, or wdtype rows)."""
+    if spec.ffn_quant:
+        fn = O.ffn_sparse_q4 if spec.ffn_q4 else O.ffn_sparse_q8
+        return fn(x, host["up_q"], host["up_s"], host.get("gate_q"), host.get("gate_s"), host["down_q"],
+                  host["down_s"], spec.act, active, perm)
     return O.ffn_sparse_stored(x, host["up"], host.get("gate"), host["down"], spec.wdtype, spec.act, active, perm)
 
 

@@ -65,10 +65,11 @@ typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_REGLU = 1, SFFN_ACT_SWIGLU = 2, SFFN_
 typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
 
 /* Storage of the FFN rows (up, gate, down): in the layer's wdtype, or as 8-bit
- * codes with one fp32 scale per neuron (weight = code x scale; the quantized
- * models the pages run, here in their 8-bit form). The predictor (W1, W2)
- * always uses wdtype. */
-typedef enum { SFFN_FFN_ROWS = 0, SFFN_FFN_Q8 = 1 } sffn_ffn_format;
+ * or 4-bit codes with one fp32 scale per neuron (weight = code x scale; the
+ * quantized models the pages run, e.g. PowerInfer's OPT-30B-Q4). SFFN_FFN_Q4
+ * stores two signed 4-bit codes per byte, element 2i in the low half of byte
+ * i. The predictor (W1, W2) always uses wdtype. */
+typedef enum { SFFN_FFN_ROWS = 0, SFFN_FFN_Q8 = 1, SFFN_FFN_Q4 = 2 } sffn_ffn_format;
 
 /* Shape of one FFN layer and its predictor.
  *   d: model dimension, multiple of 8, 8 <= d <= 16384.
@@ -85,7 +86,8 @@ typedef struct {
   int32_t wdtype;
   int32_t max_batch;
   int32_t ffn_format;   /* sffn_ffn_format; SFFN_FFN_Q8 needs wdtype fp16/bf16 and d % 16 == 0,
-                           and batched calls (B > 1) are not implemented for it */
+                           SFFN_FFN_Q4 fp16/bf16 and d % 32 == 0; batched calls (B > 1)
+                           are not implemented for either */
 } sffn_layer_desc;
 
 /* One token's (or a batch's) active-set views, all device buffers owned by the
@@ -123,7 +125,7 @@ typedef struct {
   const void* gate;
   const void* downT;
   const int32_t* perm;
-  /* SFFN_FFN_Q8 only (NULL otherwise): per-slot scales of up, gate, downT rows */
+  /* SFFN_FFN_Q8 / SFFN_FFN_Q4 only (NULL otherwise): per-slot scales of up, gate, downT rows */
   const float* up_scale;
   const float* gate_scale;
   const float* down_scale;
@@ -170,6 +172,15 @@ sffn_status sffn_layer_pack(sffn_layer* layer, const void* W1, const float* b1, 
  * aligned. Errors: INVALID_ARG (also: the layer is not SFFN_FFN_Q8), DEVICE,
  * OOM, CUDA. The plain sffn_layer_pack rejects SFFN_FFN_Q8 layers. */
 sffn_status sffn_layer_pack_q8(sffn_layer* layer, const void* W1, const float* b1, const void* W2,
+                               const float* b2, const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
+                               const float* gate_scale, const int8_t* down_q, const float* down_scale,
+                               const int32_t* perm, sffn_stream stream);
+
+/* sffn_layer_pack_q8 for an SFFN_FFN_Q4 layer: the same arguments, with every
+ * code in [-8, 7] (one int8 per code; the library packs two per byte). A code
+ * outside that range fails with DEVICE and leaves the layer unpacked.
+ * Errors: INVALID_ARG (also: the layer is not SFFN_FFN_Q4), DEVICE, OOM, CUDA. */
+sffn_status sffn_layer_pack_q4(sffn_layer* layer, const void* W1, const float* b1, const void* W2,
                                const float* b2, const int8_t* up_q, const float* up_scale, const int8_t* gate_q,
                                const float* gate_scale, const int8_t* down_q, const float* down_scale,
                                const int32_t* perm, sffn_stream stream);

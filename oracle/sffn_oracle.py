@@ -237,6 +237,35 @@ def ffn_sparse_q8(x: np.ndarray, up_q, up_scale, gate_q, gate_scale, down_q, dow
     return ffn_sparse(x, U, G, D, act, np.ones(orig.shape[0], dtype=bool), None)
 
 
+def ffn_sparse_q4(x: np.ndarray, up_q, up_scale, gate_q, gate_scale, down_q, down_scale, act: str,
+                  active: np.ndarray, perm=None) -> tuple[np.ndarray, np.ndarray]:
+    """:func:`ffn_sparse_q8` for 4-bit rows (PowerInfer's OPT-30B-Q4 runs): the
+    same weight = code x scale, with every code an int8 in [-8, 7]; the two-
+    codes-per-byte storage is an encoding (:func:`pack_q4`), not arithmetic."""
+    for q in (up_q, gate_q, down_q):
+        if q is not None and (q.min() < -8 or q.max() > 7):
+            raise ValueError("4-bit codes must lie in [-8, 7]")
+    return ffn_sparse_q8(x, up_q, up_scale, gate_q, gate_scale, down_q, down_scale, act, active, perm)
+
+
+def pack_q4(codes: np.ndarray) -> np.ndarray:
+    """Storage of 4-bit codes along the last axis (even length): byte i holds
+    code 2i in its low half and code 2i+1 in its high half, each as a 4-bit
+    two's-complement number."""
+    c = np.asarray(codes).astype(np.int16)
+    lo, hi = c[..., 0::2] & 15, c[..., 1::2] & 15
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_q4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`pack_q4`: int8 codes in [-8, 7]."""
+    b = np.asarray(packed).astype(np.int16)
+    lo, hi = b & 15, b >> 4
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.int16)
+    out[..., 0::2], out[..., 1::2] = lo, hi
+    return np.where(out >= 8, out - 16, out).astype(np.int8)
+
+
 # --------------------------------------------------------------------------
 # One layer, one or more tokens
 # --------------------------------------------------------------------------

@@ -40,7 +40,8 @@ class HostLayer:
         self.dt = wdtype
         self.W1 = O.widen(W.stored_numpy(w["W1"]), wdtype)
         self.W2 = O.widen(W.stored_numpy(w["W2"]), wdtype)
-        self.q8 = w.get("up_q") is not None     # 8-bit FFN rows: codes and per-neuron scales
+        self.q8 = w.get("up_q") is not None     # 8-bit or 4-bit FFN rows: codes and per-neuron scales
+        self.qbits = w.get("qbits", 8) if self.q8 else 0
         if self.q8:
             self.q = {k: (w[k].cpu().numpy() if w.get(k) is not None else None)
                       for k in ("up_q", "up_s", "gate_q", "gate_s", "down_q", "down_s")}
@@ -63,8 +64,9 @@ class HostLayer:
     def ffn(self, x: np.ndarray, active_slots: np.ndarray, act: str) -> np.ndarray:
         if self.q8:
             q = self.q
-            y, _ = O.ffn_sparse_q8(x, q["up_q"], q["up_s"], q["gate_q"], q["gate_s"], q["down_q"], q["down_s"], act,
-                                   active_slots, self.perm)
+            fn = O.ffn_sparse_q4 if self.qbits == 4 else O.ffn_sparse_q8
+            y, _ = fn(x, q["up_q"], q["up_s"], q["gate_q"], q["gate_s"], q["down_q"], q["down_s"], act,
+                      active_slots, self.perm)
             return y
         y, _ = O.ffn_sparse_stored(x, self.up, self.gate, self.down, self.dt, act, active_slots, self.perm)
         return y

@@ -438,3 +438,40 @@ def test_q8_all_active_equals_library_dense(act):
     down = torch.from_numpy(down_q).double() * torch.from_numpy(s_dn).double()[None, :]
     ref = _torch_dense(x, up.numpy(), gate, down.numpy(), act)
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_q4_storage_hand_computed():
+    """Codes 1, -2 -> low half 0x1, high half (-2 mod 16) = 0xE: byte 0xE1;
+    -8, 7 -> 0x8 | 0x70 = 0x78; 0, -1 -> 0xF0."""
+    b = O.pack_q4(np.array([1, -2, -8, 7, 0, -1], dtype=np.int8))
+    assert b.tolist() == [0xE1, 0x78, 0xF0]
+    assert O.unpack_q4(b).tolist() == [1, -2, -8, 7, 0, -1]
+
+
+def test_q4_storage_roundtrip_every_pair():
+    c = np.array([[a, b] for a in range(-8, 8) for b in range(-8, 8)], dtype=np.int8)
+    packed = O.pack_q4(c)
+    assert packed.shape == (256, 1) and sorted(packed[:, 0].tolist()) == list(range(256))
+    assert (O.unpack_q4(packed) == c).all()
+
+
+def test_q4_range_and_arithmetic():
+    """4-bit rows use the 8-bit arithmetic (code x scale); codes outside
+    [-8, 7] are refused."""
+    rng = np.random.default_rng(5)
+    d, f = 16, 32
+    up_q = rng.integers(-8, 8, (f, d)).astype(np.int8)
+    down_q = rng.integers(-8, 8, (d, f)).astype(np.int8)
+    s_up = rng.uniform(1e-2, 1e-1, f).astype(np.float32)
+    s_dn = rng.uniform(1e-2, 1e-1, f).astype(np.float32)
+    x = rng.standard_normal(d)
+    act = rng.random(f) < 0.5
+    y4, h4 = O.ffn_sparse_q4(x, up_q, s_up, None, None, down_q, s_dn, "relu", act)
+    U = up_q.astype(np.float64) * s_up.astype(np.float64)[:, None]
+    D = down_q.astype(np.float64) * s_dn.astype(np.float64)[None, :]
+    h = np.maximum(U[act] @ x, 0.0)
+    assert np.allclose(y4, D[:, act] @ h, rtol=1e-13, atol=1e-13) and np.allclose(h4, h, rtol=1e-13, atol=0)
+    bad = up_q.copy()
+    bad[0, 0] = 8
+    with pytest.raises(ValueError):
+        O.ffn_sparse_q4(x, bad, s_up, None, None, down_q, s_dn, "relu", act)

@@ -120,7 +120,7 @@ def test_perm_is_permutation_and_stored_dtypes():
             spec = W.spec_replace(spec, union_target=(32, 0.6))
         L = W.make_layer(spec, seed=0, layer=0)
         assert sorted(L["perm"].tolist()) == list(range(spec.f))
-        sfx = "_q" if spec.ffn_q8 else ""
+        sfx = "_q" if spec.ffn_quant else ""
         assert L["W1"].dtype == W.torch_dtype(spec.wdtype) and L["up" + sfx].shape == (spec.f, spec.d)
         assert L["down" + sfx].shape == (spec.d, spec.f)
         assert (L["gate" + sfx] is None) == (not spec.gated)
@@ -154,3 +154,20 @@ def test_q8_layer_fields():
     assert w["up_q"].shape == (512, 256) and w["gate_q"].shape == (512, 256) and w["down_q"].shape == (256, 512)
     assert w["up_s"].shape == w["gate_s"].shape == w["down_s"].shape == (512,)
     assert W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q8_8l"].fbytes == 1
+
+
+def test_quantize_rows_q4():
+    g = torch.Generator().manual_seed(1)
+    w = torch.randn(40, 64, generator=g).to(torch.bfloat16)
+    q, s = W.quantize_rows_q8(w, bits=4)
+    assert q.dtype == torch.int8 and int(q.min()) >= -7 and int(q.max()) <= 7
+    assert (q.abs().amax(dim=1) == 7).all()                 # the largest |w| of a row maps to 7
+    err = (q.float() * s[:, None] - w.float()).abs()
+    assert (err <= s[:, None] / 2 + 1e-7).all()
+
+
+def test_q4_layer_fields():
+    spec = W.spec_replace(W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q4_8l"], d=256, f=512, h=64)
+    w = W.make_layer(spec, seed=0)
+    assert w["qbits"] == 4 and w["up"] is None and int(w["down_q"].abs().max()) <= 7
+    assert spec.fbytes == 0.5 and spec.ffn_quant
