@@ -49,7 +49,7 @@ struct GemmArgs {
   int lda;                  // elements per A row
   const unsigned char* Bhl; // [2][npad][ldb] 16-bit hi then lo parts, K-major
   int ldb;
-  float* D;                 // partial tiles [slot][128][npad] (slot = CTA + tile, see Plan)
+  float* D;                 // partial tiles [slot][npad][tile rows] (slot = CTA + tile, see Plan)
   size_t dmat_stride;       // floats from the first matrix's partials to the second's
   int grid;                 // CTAs launched
   uint32_t* err;
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 0; i < NIK; ++i) {
               const uint32_t so = (uint32_t)(jb * NMAT) * kA + tc::kmajor_off(tid / TPR + RPI * i, cj);
-              tc::cp_async16(st + so, g.A0 + roff[i] + kofs);
-              if (NMAT == 2) tc::cp_async16(st + so + kA, g.A1 + roff[i] + kofs);
+              tc::cp_async16(st + so, g.A0 + roff[i] + kofs, pol_a);
+              if (NMAT == 2) tc::cp_async16(st + so + kA, g.A1 + roff[i] + kofs, pol_a);
             }
           } else {
             const int cur = nidx;
@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 0; i < NIM; ++i) {
               const int r = __shfl_sync(SFFN_FULL_MASK, cur, hbase | i);
-              tc::cp_async16(st + mi * kA + tc::mnmajor_off(k0 + RPK * i, c16), g.A0 + (size_t)r * g.lda * 2 + mofs);
+              tc::cp_async16(st + mi * kA + tc::mnmajor_off(k0 + RPK * i, c16), g.A0 + (size_t)r * g.lda * 2 + mofs,
+                             pol_a);
             }
           }
           tc::cp_async_arrive(&full[s]);
@@ -360,9 +361,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tl = tmem + ((uint32_t)(ew * 32) << 16);
 #pragma unroll
       for (int a = 0; a < NACC; ++a) {
-        // slot cta + mt; MN-major: row a * 128 + r of the slot's MSUB * 128 rows
-        float* dst = MN ? g.D + ((size_t)(cta + mt) * p.tile_rows + a * kTileM + ew * 32 + lane) * NPAD
-                        : g.D + (size_t)a * g.dmat_stride + ((size_t)(cta + mt) * kTileM + ew * 32 + lane) * NPAD;
+        // slot cta + mt, token-major: token n's value of output row r at
+        // n * tile_rows + r (MN-major: r = a * 128 + the lane's row), so each
+        // store of a warp writes 32 consecutive rows of one token
+        float* dst = MN ? g.D + (size_t)(cta + mt) * p.tile_rows * NPAD + a * kTileM + ew * 32 + lane
+                        : g.D + (size_t)a * g.dmat_stride + (size_t)(cta + mt) * kTileM * NPAD + ew * 32 + lane;
 #pragma unroll
         for (int c0 = 0; c0 < NPAD; c0 += 16) {
           float vh[16], vl[16];
@@ -370,9 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc::ld16(tl + (uint32_t)(a * N2 + NPAD + c0), vl);
           tc::wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + c0 + i) =
-                make_float4(vh[i] + vl[i], vh[i + 1] + vl[i + 1], vh[i + 2] + vl[i + 2], vh[i + 3] + vl[i + 3]);
+          for (int i = 0; i < 16; ++i) dst[(size_t)(c0 + i) * p.tile_rows] = vh[i] + vl[i];
         }
       }
       tc::fence_before();
@@ -424,81 +425,110 @@ __global__ void k_b_split(const float* in, int B, int K, int npad, T* out) {
   }
 }
 
-// The partial tiles are laid out [slot][tile_rows][npad]: one row's npad values
-// are contiguous, so the finishers below give each thread four tokens of one
-// row (a 16-byte load per partial) and let consecutive threads take
-// consecutive rows, which keeps their 16-bit outputs [npad][rows] coalesced.
+// The partial tiles are laid out token-major, [slot][npad][tile_rows]: the
+// finishers below give consecutive threads consecutive output rows of one
+// token, so every load of a warp reads 128 contiguous bytes of a partial and
+// every 16-bit output [npad][rows] is written coalesced too.
 
-// Tokens 4nq..4nq+3 of output row `row`: the partials of the CTAs that touched
-// its tile, added in CTA order (zero when the product is empty).
-__device__ __forceinline__ float4 sum_segments(const float* D, const Plan& p, int row, int npad, int nq) {
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.total == 0) return a;
+// Partials of output row `row` (tile mt = row / tile_rows): the CTAs b0..b1
+// that touched its tile, slot b + mt each.
+struct RowSlots {
+  const float* q;  // the row's value of token 0 in slot b0 + mt
+  size_t slot;     // floats per slot
+  int nb;          // b1 - b0 + 1, 0 for an empty product
+};
+
+__device__ __forceinline__ RowSlots row_slots(const float* D, const Plan& p, int row, int npad) {
+  RowSlots r;
+  r.slot = (size_t)p.tile_rows * npad;
+  r.nb = 0;
+  r.q = D;
+  if (p.total == 0) return r;
   const int mt = row / p.tile_rows, rr = row % p.tile_rows;
   const int b0 = cta_of(p, (long long)mt * p.kblocks), b1 = cta_of(p, (long long)(mt + 1) * p.kblocks - 1);
-#pragma unroll 8
-  for (int b = b0; b <= b1; ++b) {
-    const float4 v = ld_dep4(D + ((size_t)(b + mt) * p.tile_rows + rr) * npad + nq * 4);
-    a.x += v.x;
-    a.y += v.y;
-    a.z += v.z;
-    a.w += v.w;
+  r.nb = b1 - b0 + 1;
+  r.q = D + (size_t)(b0 + mt) * r.slot + rr;
+  return r;
+}
+
+// Tokens n0..n0+T-1 of the row (those below nvalid; the others stay 0): each
+// token's partials added in CTA order, the loads of KB CTAs for all T tokens
+// in flight together.
+template <int T, int KB>
+__device__ __forceinline__ void sum_partials(const RowSlots& r, int n0, int nvalid, int tile_rows, float (&acc)[T]) {
+#pragma unroll
+  for (int e = 0; e < T; ++e) acc[e] = 0.f;
+  const float* q = r.q + (size_t)n0 * tile_rows;
+  for (int b = 0; b < r.nb; b += KB) {
+    float v[KB][T];
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+#pragma unroll
+      for (int e = 0; e < T; ++e)
+        v[k][e] = b + k < r.nb && n0 + e < nvalid ? ld_dep(q + (size_t)(b + k) * r.slot + (size_t)e * tile_rows) : 0.f;
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+      if (b + k < r.nb)
+#pragma unroll
+        for (int e = 0; e < T; ++e) acc[e] += v[k][e];
   }
-  return a;
 }
 
-__device__ __forceinline__ float f4_get(const float4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
-// hid[n][j] = ReLU(sum_kq D[kq][j][n] + b1[j]) as hi/lo parts [2][npad][h].
-// Thread i = nq * h + j.
+// hid[n][j] = ReLU(sum_kq D[kq][n][j] + b1[j]) as hi/lo parts [2][npad][h].
+// Thread i = n * h + j.
 template <typename T>
 __global__ void k_b_hidden_fin(const float* D, int d, int grid, int npad, int h, int B, const float* b1, T* out) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (npad / 4) * h) return;
-  const int nq = i / h, j = i % h;
-  const Plan p = make_plan(false, h, d, grid, ksub_contig(d));  // the hidden product's plan (K = d)
-  const float4 a = sum_segments(D, p, j, npad, nq);
-  const float bias = b1 ? b1[j] : 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int n = nq * 4 + e;
-    const float v = n < B ? relu_nan(f4_get(a, e) + bias) : 0.f;
-    T hi, lo;
-    split16<T>(v, hi, lo);
-    out[(size_t)n * h + j] = hi;
-    out[(size_t)npad * h + (size_t)n * h + j] = lo;
+  if (i >= npad * h) return;
+  const int n = i / h, j = i % h;
+  float v = 0.f;
+  if (n < B) {
+    const Plan p = make_plan(false, h, d, grid, ksub_contig(d));  // the hidden product's plan (K = d)
+    float a[1];
+    sum_partials<1, 16>(row_slots(D, p, j, npad), n, B, p.tile_rows, a);
+    v = relu_nan(a[0] + (b1 ? b1[j] : 0.f));
   }
+  T hi, lo;
+  split16<T>(v, hi, lo);
+  out[(size_t)n * h + j] = hi;
+  out[(size_t)npad * h + (size_t)n * h + j] = lo;
 }
 
-// nmask[n][w] for every token n < B, and the union word unmask[w]: one warp
-// per mask word, lane = row of the word, one ballot per token.
-__global__ void k_b_scores_fin(const float* D, int h, int grid, int npad, int nw, int B, const float* b2,
-                               float thres, uint32_t* nmask, uint32_t* unmask) {
+// nmask[n][w] for every token n < B, and the union word unmask[w]. A block
+// of 256 threads takes two mask words, four warps each; lane = row of the
+// word, warp q of a word takes tokens 8q..8q+7 (one ballot per token) and the
+// four warps' unions are joined in shared memory.
+__global__ void __launch_bounds__(256)
+    k_b_scores_fin(const float* D, int h, int grid, int npad, int nw, int B, const float* b2, float thres,
+                   uint32_t* nmask, uint32_t* unmask) {
   pdl_launch_dependents();
   pdl_wait();
-  const int w = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (w >= nw) return;
-  const int row = w * 32 + lane;
-  const Plan p = make_plan(false, nw * 32, h, grid, ksub_contig(h));  // the scores product's plan (K = h)
-  const float bias = b2 ? b2[row] : 0.f;
-  uint32_t mine = 0, uni = 0;
-  for (int nq = 0; nq * 4 < B; ++nq) {
-    const float4 a = sum_segments(D, p, row, npad, nq);
+  __shared__ uint32_t s_uni[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * 2 + (warp >> 2), q = warp & 3;
+  uint32_t uni = 0;
+  if (w < nw && q * 8 < B) {
+    const int row = w * 32 + lane;
+    const Plan p = make_plan(false, nw * 32, h, grid, ksub_contig(h));  // the scores product's plan (K = h)
+    const RowSlots r = row_slots(D, p, row, npad);
+    float acc[8];
+    sum_partials<8, 4>(r, q * 8, B, p.tile_rows, acc);
+    const float bias = b2 ? b2[row] : 0.f;
+    uint32_t mine = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int n = nq * 4 + e;
-      const uint32_t m = __ballot_sync(SFFN_FULL_MASK, n < B && f4_get(a, e) + bias >= thres);  // NaN: false
-      if (lane == n) mine = m;
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t m = __ballot_sync(SFFN_FULL_MASK, q * 8 + e < B && acc[e] + bias >= thres);  // NaN: false
+      if (lane == e) mine = m;
       uni |= m;
     }
+    if (lane < 8 && q * 8 + lane < B) nmask[(size_t)(q * 8 + lane) * nw + w] = mine;
   }
-  if (lane < B) nmask[(size_t)lane * nw + w] = mine;
-  if (lane == 0) unmask[w] = uni;
+  if (lane == 0) s_uni[warp] = uni;
+  __syncthreads();
+  if ((warp & 3) == 0 && lane == 0 && w < nw)
+    unmask[w] = s_uni[warp] | s_uni[warp + 1] | s_uni[warp + 2] | s_uni[warp + 3];
 }
 
 // Views: block b < B expands token b's mask (index list, count, group mask);
@@ -545,7 +575,7 @@ __global__ void __launch_bounds__(kViewThreadsB)
 
 // H parts [2][npad][ldh]: h = act(g, u) for union neuron u and token n if the
 // neuron is in token n's own mask, else 0; zero beyond the union and for n >= B.
-// Thread i = nq * ldh + u.
+// Thread i = q * ldh + u takes tokens 8q..8q+7 of union neuron u.
 template <typename T, int ACT>
 __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32_t* ucount,
                             const int32_t* uidx, const uint32_t* nmask, int nw, int npad, int B, int ldh,
@@ -553,54 +583,66 @@ __global__ void k_b_act_fin(const float* Du, const float* Dg, int d, const int32
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (npad / 4) * ldh) return;
-  const int nq = i / ldh, u = i % ldh;
+  if (i >= (npad / 8) * ldh) return;
+  const int n0 = (i / ldh) * 8, u = i % ldh;
   const int U = ld_dep(ucount);
   if (u >= (U + kTileK - 1) / kTileK * kTileK) return;  // the down product reads no further
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  if (u < U && nq * 4 < B) {
+  float v[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = 0.f;
+  if (u < U && n0 < B) {
     const Plan p = make_plan(false, U, d, grid, ksub_gather(d, act_gated(ACT) ? 2 : 1));  // the up/gate plan
-    const float4 au = sum_segments(Du, p, u, npad, nq);
-    const float4 ag = act_gated(ACT) ? sum_segments(Dg, p, u, npad, nq) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const int slot = ld_dep(uidx + u);
+    float su[8], sg[8];
+    sum_partials<8, 4>(row_slots(Du, p, u, npad), n0, B, p.tile_rows, su);
+    if (act_gated(ACT)) {
+      sum_partials<8, 4>(row_slots(Dg, p, u, npad), n0, B, p.tile_rows, sg);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int n = nq * 4 + e;
-      if (n < B && ((ld_dep(nmask + (size_t)n * nw + (slot >> 5)) >> (slot & 31)) & 1u))
-        v[e] = neuron_act<ACT>(f4_get(au, e), f4_get(ag, e));
+      for (int e = 0; e < 8; ++e) sg[e] = 0.f;
     }
-  }
-  const size_t total = (size_t)npad * ldh;
+    const int slot = ld_dep(uidx + u);
+    uint32_t mw[8];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const size_t o = (size_t)(nq * 4 + e) * ldh + u;
+    for (int e = 0; e < 8; ++e) mw[e] = n0 + e < B ? ld_dep(nmask + (size_t)(n0 + e) * nw + (slot >> 5)) : 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if ((mw[e] >> (slot & 31)) & 1u) v[e] = neuron_act<ACT>(su[e], sg[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const size_t o = (size_t)(n0 + e) * ldh + u;
     T hi, lo;
     split16<T>(v[e], hi, lo);
     H[o] = hi;
-    H[total + o] = lo;
+    H[(size_t)npad * ldh + o] = lo;
   }
 }
 
-// y[n][c] = sum_kq D[kq][c][n]; x_out = x + y. Thread i = nq * d + c.
+// y[n][c] = sum_kq D[kq][n][c]; x_out = x + y. Thread i = q * d + c takes
+// tokens 2q and 2q + 1 of output row c.
 __global__ void k_b_y_fin(const float* D, const int32_t* ucount, int d, int npad, int B, int grid, const float* x,
                           float* y, float* x_out) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (npad / 4) * d) return;
-  const int nq = i / d, c = i % d;
-  if (nq * 4 >= B) return;
+  if (i >= (B + 1) / 2 * d) return;
+  const int n0 = (i / d) * 2, c = i % d;
+  float xv[2] = {0.f, 0.f};
+  if (x_out) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (n0 + e < B) xv[e] = ld_dep(x + (size_t)(n0 + e) * d + c);
+  }
   const int U = ld_dep(ucount);
   const Plan p = make_plan(true, U, d, grid, 1, msub_down(d));
-  const float4 a = sum_segments(D, p, c, npad, nq);
+  float s[2];
+  sum_partials<2, 8>(row_slots(D, p, c, npad), n0, B, p.tile_rows, s);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int n = nq * 4 + e;
-    if (n < B) {
-      const size_t o = (size_t)n * d + c;
-      const float s = f4_get(a, e);
-      y[o] = s;
-      if (x_out) x_out[o] = ld_dep(x + o) + s;
+  for (int e = 0; e < 2; ++e) {
+    if (n0 + e < B) {
+      const size_t o = (size_t)(n0 + e) * d + c;
+      y[o] = s[e];
+      if (x_out) x_out[o] = xv[e] + s[e];
     }
   }
 }
@@ -834,7 +876,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     if (e == cudaSuccess) e = traced_b(L, 0, st, [&] { return launch_contig(L, npad, g, st); });
     if (e != cudaSuccess) return e;
     void* hidhl = base + w.hidhl;
-    const int hb = ((npad / 4) * h + 255) / 256;
+    const int hb = (npad * h + 255) / 256;
     const float* b1 = L.has_b1 ? L.b1 : nullptr;
     if (bf)
       e = launch_ex(k_b_hidden_fin<__nv_bfloat16>, dim3(hb), dim3(256), 0, st, true, 1,
@@ -860,7 +902,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
     if (e == cudaSuccess) e = traced_b(L, 1, st, [&] { return launch_contig(L, npad, s, st); });
     if (e != cudaSuccess) return e;
     const float* b2 = L.has_b2 ? L.b2 : nullptr;
-    e = launch_ex(k_b_scores_fin, dim3((nw + 7) / 8), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D), h,
+    e = launch_ex(k_b_scores_fin, dim3((nw + 1) / 2), dim3(256), 0, st, true, 1, static_cast<const float*>(s.D), h,
                   grid, npad, nw, B, b2, thres, m->nmask, unmask);
     if (e != cudaSuccess) return e;
   }
@@ -892,7 +934,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   if (e != cudaSuccess) return e;
   // activation with each token's own mask -> H parts [2][npad][fpad]
   void* hhl = base + w.hhl;
-  const int ab = ((npad / 4) * fpad + 255) / 256;
+  const int ab = ((npad / 8) * fpad + 255) / 256;
 #define SFFN_ACT_LAUNCH(T, A)                                                                                     \
   launch_ex(k_b_act_fin<T, A>, dim3(ab), dim3(256), 0, st, true, 1, static_cast<const float*>(u.D),              \
             static_cast<const float*>(u.D + dmat), d, static_cast<const int32_t*>(ucount),                        \
@@ -921,7 +963,7 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   e = encode_rows(&dn.tmB, hhl, bf, fpad, 2 * npad, 2 * npad);
   if (e == cudaSuccess) e = traced_b(L, 3, st, [&] { return launch_down(L, npad, dn, st); });
   if (e != cudaSuccess) return e;
-  return launch_ex(k_b_y_fin, dim3(((npad / 4) * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
+  return launch_ex(k_b_y_fin, dim3(((B + 1) / 2 * d + 255) / 256), dim3(256), 0, st, true, 1, static_cast<const float*>(dn.D),
                    static_cast<const int32_t*>(ucount), d, npad, B, grid, x, y, x_out);
 }
 

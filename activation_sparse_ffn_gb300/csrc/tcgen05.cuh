@@ -84,9 +84,12 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float* v) {
 
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 16-byte asynchronous copy global -> shared through L2 (not L1).
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+// 16-byte asynchronous copy global -> shared through L2 (not L1), read under
+// the given L2 eviction policy.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+               "l"(policy)
+               : "memory");
 }
 
 // One arrival on the mbarrier once all of this thread's earlier cp.async
