@@ -531,6 +531,31 @@ __global__ void __launch_bounds__(256)
     unmask[w] = s_uni[warp] | s_uni[warp + 1] | s_uni[warp + 2] | s_uni[warp + 3];
 }
 
+// Writes the ascending active list to out (s_words / s_off from
+// scan_mask_words): warp k takes a run of consecutive words, 32 at a time with
+// one word and its list offset per lane, and walks them by shuffles; lane l
+// tests bit l of the word and the set lanes store their entries side by side
+// (list position = the word's offset + the set bits below the lane).
+__device__ __forceinline__ void extract_list_ballot(const uint32_t* s_words, const int* s_off, int nw,
+                                                    int32_t* out) {
+  constexpr int kWarps = kViewThreadsB / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (nw + kWarps - 1) / kWarps;
+  const int w0 = min(nw, warp * per), w1 = min(nw, w0 + per);
+  const uint32_t below = (1u << lane) - 1u;
+  for (int c = w0; c < w1; c += 32) {
+    const int n = min(32, w1 - c);
+    const uint32_t ml = lane < n ? s_words[c + lane] : 0u;
+    const int pl = lane < n ? s_off[c + lane] : 0;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t m = __shfl_sync(SFFN_FULL_MASK, ml, k);
+      const int p = __shfl_sync(SFFN_FULL_MASK, pl, k);
+      if ((m >> lane) & 1u) out[p + __popc(m & below)] = (c + k) * 32 + lane;
+    }
+  }
+}
+
 // Views: block b < B expands token b's mask (index list, count, group mask);
 // block B expands the union mask, forming it first (OR over tokens) unless
 // the scores finisher already wrote it (union_ready).
@@ -563,11 +588,11 @@ __global__ void __launch_bounds__(kViewThreadsB)
   }
   const int total = scan_mask_words<kViewThreadsB>(src, nw, s_words, s_off, s_tmp);
   if (b < B) {
-    if (idx) extract_slice<kViewThreadsB>(s_words, s_off, nw, 0, total, idx + (size_t)b * f);
+    if (idx) extract_list_ballot(s_words, s_off, nw, idx + (size_t)b * f);
     if (count && threadIdx.x == 0) count[b] = total;
     if (gmask) write_group_mask<kViewThreadsB>(s_words, n_groups, G, gwords, gmask + (size_t)b * gwords);
   } else {
-    extract_slice<kViewThreadsB>(s_words, s_off, nw, 0, total, uidx);
+    extract_list_ballot(s_words, s_off, nw, uidx);
     if (threadIdx.x == 0) *ucount = total;
     if (ugmask) write_group_mask<kViewThreadsB>(s_words, n_groups, G, gwords, ugmask);
   }
