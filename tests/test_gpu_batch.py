@@ -68,6 +68,11 @@ SHAPES = [
     (768, 2048, 192, 64, "reglu", "f16"),
     (384, 1024, 64, 32, "relu", "bf16"),
     (1024, 2048, 128, 64, "relu2", "f16"),
+    # the views cut each list into four slices of whole group-mask words: a
+    # ragged last slice (224 words in slices of 64) and a last group-mask word
+    # with one group (65 groups of 32)
+    (1024, 7168, 128, 64, "reglu", "bf16"),
+    (512, 2080, 64, 32, "relu", "f16"),
 ]
 
 
@@ -134,6 +139,14 @@ def test_batch_forward_with_caller_masks_and_residual(sffn):
         check_y(y[b].cpu().numpy(), host.ffn(X[b].double().cpu().numpy(), bits[b], "relu"), "bf16", f"y[{b}]")
     assert torch.equal(xo, X + y)
     assert (y[0] == 0).all()
+    # the union views, formed here from the caller's masks
+    union = bits.any(axis=0)
+    assert np.array_equal(words_bits(masks.unmask.cpu().numpy(), spec.f), union)
+    uc = masks.ucount.item()
+    assert uc == int(union.sum())
+    assert np.array_equal(masks.uidx[:uc].cpu().numpy(), np.flatnonzero(union))
+    ng = spec.f // spec.group_size
+    assert np.array_equal(words_bits(masks.ugmask.cpu().numpy(), ng), union.reshape(ng, -1).any(axis=1))
     L.check_error()
 
 
