@@ -83,6 +83,8 @@ WsLayout ws_layout(const sffn_layer& L, int B) {
   off = align256(off + (size_t)B * L.desc.h * 4);
   w.partials = off;
   off = align256(off + (size_t)B * ffn_blocks(L) * L.desc.d * 4);
+  w.kept = off;
+  off = align256(off + (size_t)ffn_blocks(L) * 4);
   w.total = off;
   return w;
 }
@@ -303,6 +305,14 @@ sffn_status sffn_layer_set_grid(sffn_layer* L, int32_t ffn_blocks, int32_t score
   return SFFN_OK;
 }
 
+sffn_status sffn_layer_set_zero_skip(sffn_layer* L, int32_t enable, int32_t* rows_read) {
+  if (!L) return invalid("layer is NULL");
+  if (rows_read && !aligned(rows_read, 4)) return invalid("rows_read must be 4-byte aligned");
+  L->zero_skip = enable != 0;
+  L->rows_read = enable ? rows_read : nullptr;
+  return SFFN_OK;
+}
+
 sffn_status sffn_layer_set_l2_resident(sffn_layer* L, const uint32_t* resident) {
   if (!L) return invalid("layer is NULL");
   if (resident && (reinterpret_cast<uintptr_t>(resident) & 3)) return invalid("resident must be 4-byte aligned");
@@ -403,8 +413,10 @@ sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const s
   const WsLayout w = ws_layout(*L, B);
   char* base = static_cast<char*>(ws);
   float* part = reinterpret_cast<float*>(base + w.partials);
-  cudaError_t e = traced(*L, 2, st, [&] { return launch_ffn(*L, x, m->nmask, nullptr, nullptr, nullptr, part, st); });
-  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, x, y, x_out, st); });
+  int32_t* kept = reinterpret_cast<int32_t*>(base + w.kept);
+  cudaError_t e =
+      traced(*L, 2, st, [&] { return launch_ffn(*L, x, m->nmask, nullptr, nullptr, nullptr, part, kept, st); });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, kept, x, y, x_out, st); });
   if (e != cudaSuccess) return cuda_fail(e, "sffn_forward: launch");
   return SFFN_OK;
 }
@@ -426,13 +438,14 @@ sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, flo
   char* base = static_cast<char*>(ws);
   float* hid = reinterpret_cast<float*>(base + w.hid);
   float* part = reinterpret_cast<float*>(base + w.partials);
+  int32_t* kept = reinterpret_cast<int32_t*>(base + w.kept);
   cudaError_t e = traced(*L, 0, st, [&] { return launch_pred_hidden(*L, x, hid, st); });
   if (e == cudaSuccess) e = traced(*L, 1, st, [&] { return launch_pred_scores(*L, hid, thres, m->nmask, st); });
   if (e == cudaSuccess)
     e = traced(*L, 2, st, [&] {
-      return launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, st);
+      return launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, kept, st);
     });
-  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, x, y, x_out, st); });
+  if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, kept, x, y, x_out, st); });
   if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
   return SFFN_OK;
 }

@@ -15,6 +15,9 @@
 // activation gives h. Phase B: the same chunk ownership accumulates
 // h_i * downT_i into per-thread registers, so the block ends with a partial of
 // y over its neurons, written to the workspace.
+// Zero-skip (optional): the consumers list the local neurons whose h is not
+// zero and publish the list through an mbarrier; the producer streams phase B
+// over that list only (a neuron with h = 0 adds nothing to y).
 // k_ffn_reduce adds the blocks' partials in a fixed order (no atomics) and
 // writes y and the residual x + y. Results are bit-identical run to run.
 #include "common.cuh"
@@ -58,7 +61,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, uint32_t* __restrict__ gmask_out,
           float* __restrict__ partials, uint32_t* __restrict__ err, const unsigned char* pf, size_t pf_bytes,
           const float* __restrict__ up_s, const float* __restrict__ gate_s, const float* __restrict__ down_s,
-          const uint32_t* resident) {
+          const uint32_t* resident, bool zero_skip, int32_t* __restrict__ kept) {
   constexpr int NT = kFfnThreads;
   constexpr int EPC = WType<T>::kPerChunk;
   constexpr bool GATED = act_gated(ACT);
@@ -82,6 +85,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   __shared__ int s_tmp[NT / 32];
   __shared__ int s_abort;
   __shared__ uint32_t s_res[32];  // L2-resident groups (at most 1024)
+  __shared__ uint64_t s_hready;    // zero-skip: the kept list is published
+  __shared__ int s_nkeep;          // zero-skip: neurons in the kept list
+  __shared__ int s_wcnt[kConsumerWarps];
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -89,6 +95,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(&s_hready, 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -110,6 +117,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
 
   const int nA = (n_local + NPS - 1) / NPS;                  // phase A stages: NPS neurons' up [+ gate]
   const int nB = (n_local + NMAT * NPS - 1) / (NMAT * NPS);  // phase B stages: NMAT * NPS downT rows
+  // zero-skip: phase B reads the rows of the kept list, written over s_part
+  // once the activations are known (s_part is not read after that)
+  const int32_t* s_keep = reinterpret_cast<const int32_t*>(s_part);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == kConsumerWarps) {
     // ---------------- producer
@@ -120,9 +130,18 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         const int g = slot / G;
         return (s_res[g >> 5] >> (g & 31)) & 1u ? pol_keep : pol_stream;
       };
-      for (int u = 0; u < nA + nB; ++u) {
+      int nBp = nB;  // zero-skip: known once the consumers publish the kept list
+      for (int u = 0; u < nA + nBp; ++u) {
         const int s = u % stages;
-        const bool ok = u < stages || mbar_wait_bounded(&empty[s], (uint32_t)((u / stages - 1) & 1));
+        bool ok = true;
+        if (zero_skip && u == nA) {
+          ok = mbar_wait_bounded(&s_hready, 0u);
+          if (ok) {
+            nBp = (*(volatile int*)&s_nkeep + NMAT * NPS - 1) / (NMAT * NPS);
+            if (nBp == 0) break;
+          }
+        }
+        ok = ok && (u < stages || mbar_wait_bounded(&empty[s], (uint32_t)((u / stages - 1) & 1)));
         if (!ok || *(volatile int*)&s_abort) {
           if (!ok) set_device_error(err, SFFN_ERR_TIMEOUT);
           atomicExch(&s_abort, 1);
@@ -145,12 +164,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
           }
         } else {
           const int r0 = (u - nA) * NMAT * NPS;
-          const int nr = min(NMAT * NPS, n_local - r0);
+          const int nr = min(NMAT * NPS, (zero_skip ? *(volatile int*)&s_nkeep : n_local) - r0);
           mbar_arrive_expect_tx(&full[s], (uint32_t)nr * row_bytes);
-          for (int i = 0; i < nr; ++i)
-            bulk_g2s(dst + (size_t)i * row_bytes,
-                     reinterpret_cast<const unsigned char*>(downT) + (size_t)s_list[r0 + i] * row_bytes, row_bytes,
-                     &full[s], pol_of(s_list[r0 + i]));
+          for (int i = 0; i < nr; ++i) {
+            const int slot = s_list[zero_skip ? s_keep[r0 + i] : r0 + i];
+            bulk_g2s(dst + (size_t)i * row_bytes, reinterpret_cast<const unsigned char*>(downT) + (size_t)slot * row_bytes,
+                     row_bytes, &full[s], pol_of(slot));
+          }
         }
       }
       // L2 hint: once this block's rows are all requested, its share of the
@@ -242,6 +262,34 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       if (idx_out) idx_out[lo + a] = s_list[a];
     }
     consumer_barrier();
+    int nkeep = n_local;  // neurons phase B reads
+    if (zero_skip) {
+      // the kept list: local neurons with h != 0 (NaN kept), ascending
+      int32_t* keep = reinterpret_cast<int32_t*>(s_part);
+      nkeep = 0;
+      for (int base = 0; base < n_local; base += kConsumers) {
+        const int a = base + threadIdx.x;
+        const bool k = a < n_local && s_h[a] != 0.f;
+        const uint32_t bal = __ballot_sync(SFFN_FULL_MASK, k);
+        if (lane == 0) s_wcnt[warp] = __popc(bal);
+        consumer_barrier();
+        int off = nkeep, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          off += w < warp ? s_wcnt[w] : 0;
+          tot += s_wcnt[w];
+        }
+        if (k) keep[off + __popc(bal & ((1u << lane) - 1u))] = a;
+        nkeep += tot;
+        consumer_barrier();
+      }
+      if (threadIdx.x == 0) {
+        s_nkeep = nkeep;
+        if (kept) kept[b] = nkeep;
+        mbar_arrive(&s_hready);  // release: the list and its length to the producer
+      }
+    }
+    const int nBc = (nkeep + NMAT * NPS - 1) / (NMAT * NPS);
     // ---------------- phase B: acc += h_i * downT_i over this block's neurons
     float acc[CPT][QS ? 1 : EPC];
     float2 accp[CPT][QS ? EPC / 2 : 1];  // coded rows: pairs
@@ -253,7 +301,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       for (int e = 0; e < (QS ? EPC / 2 : 1); ++e) accp[j][e] = make_float2(0.f, 0.f);
     }
     if (!__any_sync(SFFN_FULL_MASK, *(volatile int*)&s_abort)) {
-      for (int v = 0; v < nB; ++v) {
+      for (int v = 0; v < nBc; ++v) {
         const int u = nA + v;
         const int s = u % stages;
         const bool ok = __all_sync(SFFN_FULL_MASK, mbar_wait_bounded(&full[s], (uint32_t)((u / stages) & 1)));
@@ -266,9 +314,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         }
         const unsigned char* sp = ring + (size_t)s * stage_bytes;
         const int r0 = v * NMAT * NPS;
-        const int nr = min(NMAT * NPS, n_local - r0);
+        const int nr = min(NMAT * NPS, nkeep - r0);
         for (int i = 0; i < nr; ++i) {
-          const float hv = s_h[r0 + i];
+          const float hv = s_h[zero_skip ? s_keep[r0 + i] : r0 + i];
 #pragma unroll
           for (int j = 0; j < CPT; ++j) {
             const int c = threadIdx.x + j * kConsumers;
@@ -322,7 +370,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
 template <int PER>
 __global__ void __launch_bounds__(kReduceThreads)
     k_ffn_reduce(const float* partials, int nparts, int d, const float* x, float* __restrict__ y,
-                 float* __restrict__ x_out) {
+                 float* __restrict__ x_out, const int32_t* kept, int32_t* __restrict__ rows_read) {
   pdl_launch_dependents();
   pdl_wait();  // the partials come from the previous kernel
   constexpr int CG = kReduceCols / 4;             // float4 column groups per block
@@ -356,12 +404,21 @@ __global__ void __launch_bounds__(kReduceThreads)
       *reinterpret_cast<float4*>(x_out + col) = make_float4(xv.x + sum.x, xv.y + sum.y, xv.z + sum.z, xv.w + sum.w);
     }
   }
+  // zero-skip: the downT rows the FFN blocks read (one warp of the last block;
+  // an integer sum, so its order does not matter)
+  if (rows_read && blockIdx.x == gridDim.x - 1 && threadIdx.x < 32) {
+    int n = 0;
+    for (int i = threadIdx.x; i < nparts; i += 32) n += ld_dep(kept + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(SFFN_FULL_MASK, n, o);
+    if (threadIdx.x == 0) *rows_read = n;
+  }
 }
 
 template <typename T, int ACT>
 cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, cudaStream_t st, const float* x,
                          const uint32_t* nmask, int list_cap, int32_t* idx_out, int32_t* count_out,
-                         uint32_t* gmask_out, float* partials) {
+                         uint32_t* gmask_out, float* partials, int32_t* kept) {
   const T* up = static_cast<const T*>(L.up);
   const T* gate = static_cast<const T*>(L.gate);
   const T* downT = static_cast<const T*>(L.downT);
@@ -374,7 +431,7 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
 #define SFFN_FFN_ARGS                                                                                         \
   grid, dim3(kFfnThreads), smem, st, true, 1, up, gate, downT, x, nmask, L.nwords, L.n_groups,                \
       L.desc.group_size, L.gwords, L.desc.d, L.ffn_stages, list_cap, idx_out, count_out, gmask_out, partials, L.err, pf, pf_bytes, L.up_s, L.gate_s, L.down_s, \
-      L.l2_resident
+      L.l2_resident, L.zero_skip, L.zero_skip ? kept : nullptr
   switch (cpt) {
     case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
     case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);
@@ -460,7 +517,7 @@ cudaError_t configure_kernels(sffn_layer& L) {
 
 
 cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
-                       int32_t* count_out, uint32_t* gmask_out, float* partials, cudaStream_t st) {
+                       int32_t* count_out, uint32_t* gmask_out, float* partials, int32_t* kept, cudaStream_t st) {
   const dim3 grid(ffn_blocks(L));
   const size_t smem = ffn_smem(L);
   const int cpt = ffn_cpt(L), cap = ffn_list_cap(L);
@@ -468,16 +525,16 @@ cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmas
   switch (L.desc.act) {                                                                                      \
     case SFFN_ACT_RELU:                                                                                      \
       return launch_ffn_t<T, SFFN_ACT_RELU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,        \
-                                            gmask_out, partials);                     \
+                                            gmask_out, partials, kept);               \
     case SFFN_ACT_REGLU:                                                                                     \
       return launch_ffn_t<T, SFFN_ACT_REGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
-                                             gmask_out, partials);                    \
+                                             gmask_out, partials, kept);              \
     case SFFN_ACT_RELU2:                                                                                     \
       return launch_ffn_t<T, SFFN_ACT_RELU2>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,       \
-                                             gmask_out, partials);                    \
+                                             gmask_out, partials, kept);              \
     default:                                                                                                 \
       return launch_ffn_t<T, SFFN_ACT_SWIGLU>(L, cpt, grid, smem, st, x, nmask, cap, idx_out, count_out,      \
-                                              gmask_out, partials);                   \
+                                              gmask_out, partials, kept);             \
   }
   if (L.desc.ffn_format == SFFN_FFN_Q4) {
     SFFN_FFN_DISPATCH(q4x2_t)
@@ -493,17 +550,21 @@ cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmas
 #undef SFFN_FFN_DISPATCH
 }
 
-cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const float* x, float* y, float* x_out,
-                              cudaStream_t st) {
+cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const int32_t* kept, const float* x,
+                              float* y, float* x_out, cudaStream_t st) {
   const dim3 grid((L.desc.d + kReduceCols - 1) / kReduceCols), block(kReduceThreads);
   const int nparts = ffn_blocks(L);
   const int per = (nparts + kReduceGroups - 1) / kReduceGroups;
+  int32_t* rows_read = L.zero_skip ? L.rows_read : nullptr;
   if (per <= 4)
-    return launch_ex(k_ffn_reduce<4>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+    return launch_ex(k_ffn_reduce<4>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out, kept,
+                     rows_read);
   if (per <= 8)
-    return launch_ex(k_ffn_reduce<8>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+    return launch_ex(k_ffn_reduce<8>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out, kept,
+                     rows_read);
   if (per <= 16)
-    return launch_ex(k_ffn_reduce<16>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out);
+    return launch_ex(k_ffn_reduce<16>, grid, block, 0, st, true, 1, partials, nparts, L.desc.d, x, y, x_out, kept,
+                     rows_read);
   return cudaErrorNotSupported;  // more than 512 blocks: not reached on current GPUs
 }
 

@@ -44,6 +44,10 @@ struct sffn_layer {
   const sffn_layer* next = nullptr;
   // optional hot-group set (sffn_layer_set_l2_resident): device bitset [gwords]
   const uint32_t* l2_resident = nullptr;
+  // optional zero-skip (sffn_layer_set_zero_skip): downT rows only for h != 0,
+  // and where to write how many were read (device, may be null)
+  bool zero_skip = false;
+  int32_t* rows_read = nullptr;
   // optional timing hooks (sffn_layer_set_trace)
   cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -76,6 +80,7 @@ constexpr int kScoreSmemBudget = 192 * 1024;
 struct WsLayout {
   size_t hid = 0;       // float [B][h]
   size_t partials = 0;  // float [B][ffn blocks][d]: per-block partial sums of y
+  size_t kept = 0;      // int32 [ffn blocks]: downT rows each block read (zero-skip)
   size_t total = 0;
 };
 WsLayout ws_layout(const sffn_layer& L, int B);
@@ -100,10 +105,11 @@ cudaError_t launch_pred_scores(const sffn_layer& L, const float* hid, float thre
                                cudaStream_t st);
 cudaError_t launch_mask_views(const sffn_layer& L, const uint32_t* nmask, int32_t* idx, int32_t* count,
                               uint32_t* gmask, cudaStream_t st);
+// `kept`: the workspace's per-block downT row counts (written and summed under zero-skip only).
 cudaError_t launch_ffn(const sffn_layer& L, const float* x, const uint32_t* nmask, int32_t* idx_out,
-                       int32_t* count_out, uint32_t* gmask_out, float* partials, cudaStream_t st);
-cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const float* x, float* y, float* x_out,
-                              cudaStream_t st);
+                       int32_t* count_out, uint32_t* gmask_out, float* partials, int32_t* kept, cudaStream_t st);
+cudaError_t launch_ffn_reduce(const sffn_layer& L, const float* partials, const int32_t* kept, const float* x,
+                              float* y, float* x_out, cudaStream_t st);
 cudaError_t launch_tam_update(tam_state& S, int layer0, int n_layers, const uint32_t* gmask, int gstride,
                               float lambda, float eps, int K, const tam_outputs& out, cudaStream_t st);
 cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8_t* stall, float alpha,

@@ -108,10 +108,11 @@ extern "C" sffn_status sffn_decode_step_static_ws(const sffn_layer* L, const flo
   char* base = static_cast<char*>(ws);
   float* hid = reinterpret_cast<float*>(base + w.hid);
   float* part = reinterpret_cast<float*>(base + w.partials);
+  int32_t* kept = reinterpret_cast<int32_t*>(base + w.kept);
   e = launch_pred_hidden(*L, x, hid, st);
   if (e == cudaSuccess) e = launch_pred_scores(*L, hid, thres, m->nmask, st);
-  if (e == cudaSuccess) e = launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, st);
-  if (e == cudaSuccess) e = launch_ffn_reduce(*L, part, x, y, x_out, st);
+  if (e == cudaSuccess) e = launch_ffn(*L, x, m->nmask, m->idx, m->count, m->gmask, part, kept, st);
+  if (e == cudaSuccess) e = launch_ffn_reduce(*L, part, kept, x, y, x_out, st);
   if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step_static_ws: launch");
   return SFFN_OK;
 }

@@ -95,6 +95,7 @@ _sig("sffn_layer_pack_q8", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
 _sig("sffn_layer_pack_q4", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
 _sig("sffn_layer_set_l2_resident", _c, _vp, _vp)
+_sig("sffn_layer_set_zero_skip", _c, _vp, _i32, _vp)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
 _sig("sffn_layer_destroy", None, _vp)
 _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
@@ -114,7 +115,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
-    "sffn_layer_set_l2_resident",
+    "sffn_layer_set_l2_resident", "sffn_layer_set_zero_skip",
     "sffn_layer_pack_q8", "sffn_layer_pack_q4",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
@@ -249,6 +250,11 @@ def sffn_layer_set_grid(layer, ffn_blocks: int = 0, score_blocks: int = 0) -> No
 def sffn_layer_set_l2_resident(layer, resident=None) -> None:
     """Hot-group bitset (device uint32 [ceil(n_groups/32)], or None) whose rows stay in L2."""
     _check(_lib.sffn_layer_set_l2_resident(layer, _ptr(resident)), "sffn_layer_set_l2_resident")
+
+
+def sffn_layer_set_zero_skip(layer, enable: bool, rows_read=None) -> None:
+    """Zero-skip of the B = 1 FFN (downT rows of neurons with h != 0 only); rows_read: device int32 or None."""
+    _check(_lib.sffn_layer_set_zero_skip(layer, 1 if enable else 0, _ptr(rows_read)), "sffn_layer_set_zero_skip")
 
 
 def sffn_workspace_bytes(layer, B: int) -> int:
@@ -431,6 +437,11 @@ class Layer:
         """Hot-group bitset (device tensor or pointer) of sffn_layer_set_l2_resident; keeps a tensor alive."""
         sffn_layer_set_l2_resident(self.handle, resident)
         self._resident = resident
+
+    def set_zero_skip(self, enable: bool, rows_read=None) -> None:
+        """sffn_layer_set_zero_skip; keeps a rows_read tensor alive while set."""
+        sffn_layer_set_zero_skip(self.handle, enable, rows_read)
+        self._rows_read = rows_read if enable else None
 
     def set_next(self, other: "Layer | None") -> None:
         """L2 hint of sffn_layer_set_next; keeps ``other`` alive while set."""

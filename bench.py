@@ -61,6 +61,9 @@ def parse_args():
     p.add_argument("--l2-resident-mb", type=float, default=0.0, metavar="MB",
                    help="B = 1: L2 share (all layers) for the rows of hot neuron groups, which a second momentum "
                         "state sized to that share picks each token; 0 = off")
+    p.add_argument("--zero-skip", action="store_true",
+                   help="B = 1: read the downT rows of predicted-active neurons with h != 0 only (actual-activation "
+                        "zero-skip); the byte counts then count the rows read")
     p.add_argument("--no-prefetch-next", action="store_true",
                    help="do not let each layer prefetch the next layer's predictor weights into L2")
     p.add_argument("--ref-max-steps", type=int, default=24)
@@ -225,22 +228,24 @@ def batch_layer_cost(spec, ucount: int, B: int, with_b2: bool) -> dict:
     return {"kernels": k, "flops": flops, "metric": metric}
 
 
-def layer_bytes(spec, count: int, with_b2: bool) -> dict:
+def layer_bytes(spec, count: int, with_b2: bool, kept: int | None = None) -> dict:
     """Algorithmic bytes of one layer-token, per kernel: the weight rows the
-    method must read plus the small vectors each kernel must move."""
+    method must read plus the small vectors each kernel must move. kept: with
+    zero-skip, the downT rows read (neurons with h != 0); None reads all."""
     d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
-    # bytes of one active neuron's FFN rows (plus their scales for 8-bit rows)
-    row = spec.n_mats * (int(d * spec.fbytes) + (4 if spec.ffn_quant else 0))
+    # bytes of one FFN row (plus its scale for 8-bit and 4-bit rows)
+    one = int(d * spec.fbytes) + (4 if spec.ffn_quant else 0)
+    rows = count * spec.n_mats * one if kept is None else count * (spec.n_mats - 1) * one + kept * one
     k = {
         "pred_hidden": h * d * wb + d * 4 + h * 4,
         "pred_scores": f * h * wb + h * 4 + f // 8 + (f * 4 if with_b2 else 0),
         # active up/gate/down rows + x + mask words (the per-block partials stay in L2)
-        "ffn": count * row + d * 4 + f // 8,
+        "ffn": rows + d * 4 + f // 8,
         # x read, y and x + y written (partials read from L2 are not HBM traffic)
         "ffn_reduce": 3 * d * 4,
     }
-    # the metric: predictor weights + all rows of active neurons + x + y
-    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + count * row + 2 * d * 4
+    # the metric: predictor weights + the FFN rows read + x + y
+    metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + rows + 2 * d * 4
     return {"kernels": k, "metric": metric}
 
 
@@ -296,6 +301,14 @@ def run_ours(args, world, rank, local):
     # L2 hint: each layer's FFN kernel warms the next layer's predictor weights
     # (the last layer warms layer 0 for the next token)
     prefetch_next = Bt == 1 and not args.no_prefetch_next
+    # actual-activation zero-skip: each layer reports the downT rows it read
+    zero_skip = bool(args.zero_skip)
+    if zero_skip and Bt != 1:
+        raise SystemExit("--zero-skip applies to B = 1")
+    rows_read = torch.zeros(nL, dtype=torch.int32, device=dev) if zero_skip else None
+    if zero_skip:
+        for l in range(nL):
+            layers[l].set_zero_skip(True, rows_read[l:l + 1])
     if prefetch_next:
         for l in range(nL):
             layers[l].set_next(layers[(l + 1) % nL])
@@ -404,6 +417,7 @@ def run_ours(args, world, rank, local):
     # ---- census: active counts per (token, layer); deterministic given the token
     counts = np.zeros((P, nL), dtype=np.int64)       # active (B = 1) or union (B > 1) neurons
     tok_counts = np.zeros((P, nL), dtype=np.int64)   # sum over tokens of their own active neurons
+    kept = np.zeros((P, nL), dtype=np.int64)         # zero-skip: downT rows read
     la_hits = la_exact = la_extra = 0   # look-ahead vs exact masks along the same trajectory
     ex_masks = layers[0].masks(1, device=dev) if lookahead else None
 
@@ -427,16 +441,21 @@ def run_ours(args, world, rank, local):
             if Bt == 1:
                 counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
                 tok_counts[t] = counts[t]
+                if zero_skip:
+                    kept[t] = rows_read.cpu().numpy()
             else:
                 counts[t] = torch.stack([m.ucount[0] for m in masks]).cpu().numpy()
                 tok_counts[t] = torch.stack([m.count.sum() for m in masks]).cpu().numpy()
     for L in layers:
         L.check_error(stream)
 
-    def cost(c):
-        return layer_bytes(spec, c, with_b2) if Bt == 1 else batch_layer_cost(spec, c, Bt, with_b2)
+    def cost(t_, l_):
+        c = int(counts[t_, l_])
+        if Bt > 1:
+            return batch_layer_cost(spec, c, Bt, with_b2)
+        return layer_bytes(spec, c, with_b2, int(kept[t_, l_]) if zero_skip else None)
 
-    metric_bytes = np.array([[cost(int(counts[t, l]))["metric"] for l in range(nL)] for t in range(P)]).sum(axis=1)
+    metric_bytes = np.array([[cost(t, l)["metric"] for l in range(nL)] for t in range(P)]).sum(axis=1)
 
     # ---- graphs: one per distinct token
     graphs = None
@@ -512,11 +531,11 @@ def run_ours(args, world, rank, local):
     per_kernel = {}
     for k in KN:
         durs = [ev[k][r][l][0].elapsed_time(ev[k][r][l][1]) for r in range(R) for l in range(nL)]
-        kb = [cost(int(counts[r % P, l]))["kernels"][k] for r in range(R) for l in range(nL)]
+        kb = [cost(r % P, l)["kernels"][k] for r in range(R) for l in range(nL)]
         per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
                          "gbs": sum(kb) / (sum(durs) / 1e3) / 1e9}
         if Bt > 1:
-            kf = [cost(int(counts[r % P, l]))["flops"][k] for r in range(R) for l in range(nL)]
+            kf = [cost(r % P, l)["flops"][k] for r in range(R) for l in range(nL)]
             per_kernel[k]["tflops"] = sum(kf) / (sum(durs) / 1e3) / 1e12
     tam_us = 1e3 * sum(a.elapsed_time(b) for a, b in tam_ev) / R
     dom = max(KN, key=lambda k: per_kernel[k]["us"])
@@ -526,6 +545,9 @@ def run_ours(args, world, rank, local):
     # reference: the same FFN as cuBLAS GEMVs on the packed weights (torch
     # matmul with 16-bit x, fp32 accumulation inside cuBLAS), for context.
     nd = 20
+    for L in layers:   # the dense run reads every row
+        if zero_skip:
+            L.set_zero_skip(False)
     dense_masks = [layers[l].masks(Bt, device=dev) for l in range(nL)]
     for m in dense_masks:
         m.nmask.fill_(-1)
@@ -571,6 +593,9 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         dense_lib_us = 1e3 * e0.elapsed_time(e1) / nd
         del views
+    if zero_skip:
+        for l in range(nL):
+            layers[l].set_zero_skip(True, rows_read[l:l + 1])
 
     # ---- end to end through the public API with host buffers
     Xh = X.cpu().pin_memory()
@@ -608,7 +633,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peaks()
     pk = per_kernel[dom]
     dom_traffic = None
-    if Bt == 1:
+    if Bt == 1 and not zero_skip:  # the stored counters are of the kernel without zero-skip
         t = measured_traffic(dom, float(counts.mean()), prefetch_next)
         dom_traffic = round(t) if t is not None else None
     active_frac = float(tok_counts.mean() / Bt / spec.f)
@@ -631,6 +656,7 @@ def run_ours(args, world, rank, local):
             "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
             "distinct_tokens": P, "graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
             "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
+            "zero_skip": zero_skip,
             "l2": "inputs larger than L2: each step reads %.2f GB of distinct weights" % (timed_bytes / args.steps / 1e9),
             "parallelism": "replicas" if world > 1 else "single",
         },
@@ -656,6 +682,9 @@ def run_ours(args, world, rank, local):
     if replicas_note:
         line["config"]["replicas"] = replicas_note
     line["census"] = {"distinct_tokens": P, "active_count_token0_by_layer": [int(c) for c in counts[0]]}
+    if zero_skip:
+        line["zero_skip"] = {"down_rows_read_frac": round(float(kept.sum() / max(1, counts.sum())), 5),
+                             "note": "bytes count the downT rows read (neurons with h != 0), all up/gate rows"}
     if lookahead:
         line["config"]["mode"] = "one-layer-ahead prediction (layer l+1 predicted from layer l's input)"
         line["config"]["sm_split"] = {"predictor": lookahead, "ffn": n_sms - lookahead}

@@ -247,6 +247,22 @@ sffn_status sffn_layer_set_next(sffn_layer* layer, const sffn_layer* next /* or 
  * Errors: INVALID_ARG (layer NULL, resident not 4-byte aligned). */
 sffn_status sffn_layer_set_l2_resident(sffn_layer* layer, const uint32_t* resident /* device, or NULL */);
 
+/* Optional actual-activation zero-skip (PowerInfer §5.4: a neuron-aware
+ * operator checks whether a neuron is active and computes only the active
+ * ones, here applied to the activation itself). With enable != 0, the B = 1
+ * sparse FFN (sffn_forward, sffn_decode_step) reads the transposed-down row of
+ * a predicted-active neuron only if its activation h is non-zero (ReLU or a
+ * ReGLU gate that clamps to 0 gives h = 0, and h * downT_i adds nothing to y).
+ * The up (and gate) rows of every predicted-active neuron are still read: h is
+ * known only after them. y is unchanged up to the sign of a zero sum;
+ * idx / count / gmask still describe the predicted mask. rows_read: optional
+ * device int32, or NULL; each B = 1 FFN call then writes the number of
+ * transposed-down rows it read (stream-ordered with the call). Off by default;
+ * calls with B > 1 ignore it. The caller keeps rows_read alive while it is
+ * set. Host only. Errors: INVALID_ARG (layer NULL, rows_read not 4-byte
+ * aligned). */
+sffn_status sffn_layer_set_zero_skip(sffn_layer* layer, int32_t enable, int32_t* rows_read /* device, or NULL */);
+
 /* Optional B = 1 grid sizes, for running one layer's predictor and another
  * layer's sparse FFN at the same time on two streams (one-layer-ahead
  * prediction: KAIROX observes that adjacent layers see near-identical inputs,

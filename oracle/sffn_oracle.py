@@ -203,6 +203,26 @@ def ffn_sparse(x: np.ndarray, up: np.ndarray, gate: np.ndarray | None, down: np.
     return y, h
 
 
+def ffn_sparse_zero_skip(x: np.ndarray, up: np.ndarray, gate: np.ndarray | None, down: np.ndarray,
+                         act: str, active: np.ndarray, perm: np.ndarray | None = None) -> tuple[np.ndarray, int]:
+    """Zero-skip form of :func:`ffn_sparse`: the neuron-aware operator computes
+    only the neurons that matter (PowerInfer §5.4), taken one step further to
+    the activation itself. h is computed for every predicted-active neuron
+    (its up and gate rows are read), then only the down columns of neurons
+    with h_i != 0 are read (a NaN h is kept: it is not zero). Same arguments as
+    ffn_sparse. Returns (y (d,), number of down columns read)."""
+    f = up.shape[0]
+    if perm is None:
+        perm = np.arange(f)
+    orig = np.asarray(perm)[np.flatnonzero(active)]
+    u = up[orig] @ x
+    g = gate[orig] @ x if gate is not None else None
+    h = activation(act, u, g)
+    keep = h != 0.0
+    y = down[:, orig[keep]] @ h[keep]
+    return y, int(keep.sum())
+
+
 def ffn_sparse_stored(x: np.ndarray, up_s, gate_s, down_s, dtype: str, act: str, active: np.ndarray,
                       perm=None) -> tuple[np.ndarray, np.ndarray]:
     """:func:`ffn_sparse` on STORED weights (see :func:`widen`), widening only

@@ -95,6 +95,7 @@ def test_null_handles_are_rejected_on_the_host(lib):
     assert L.sffn_layer_set_next(None, None) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_layer_set_grid(None, 0, 0) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_layer_set_l2_resident(None, None) == lib.SFFN_ERR_INVALID_ARG
+    assert L.sffn_layer_set_zero_skip(None, 1, None) == lib.SFFN_ERR_INVALID_ARG
     out = ctypes.c_void_p()
     assert L.sffn_layer_create(None, ctypes.byref(out)) == lib.SFFN_ERR_INVALID_ARG
     bad = lib.make_desc(100, 2048, 64, 32, "relu", "f32")

@@ -207,6 +207,55 @@ def test_brute_force_masks_d8(f, act):
             assert np.allclose(y12, y + y2, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- zero-skip
+
+def test_zero_skip_hand_computed():
+    """d = 2, f = 4, x = (1, 2); h and y worked out by hand."""
+    x = np.array([1.0, 2.0])
+    down = np.array([[1.0, 2.0, 3.0, 4.0], [5.0, 6.0, 7.0, 8.0]])
+    up = np.array([[1.0, 0.0], [-1.0, 0.0], [0.0, 0.0], [1.0, 1.0]])       # u = (1, -1, 0, 3)
+    allon = np.ones(4, dtype=bool)
+    y, n = O.ffn_sparse_zero_skip(x, up, None, down, "relu", allon)       # h = (1, 0, 0, 3)
+    assert n == 2 and np.array_equal(y, [1 + 12, 5 + 24])
+    y, n = O.ffn_sparse_zero_skip(x, up, None, down, "relu2", allon)      # h = (1, 0, 0, 9)
+    assert n == 2 and np.array_equal(y, [1 + 36, 5 + 72])
+    # slots 0, 2, 3 active: h = (1, 0, 3) -> two columns
+    y, n = O.ffn_sparse_zero_skip(x, up, None, down, "relu", np.array([True, False, True, True]))
+    assert n == 2 and np.array_equal(y, [13, 29])
+    # ReGLU: g = (-1, 1, 3, -2), u = (2, 5, -1, 4) -> h = (0, 5, -3, 0)
+    gate = np.array([[-1.0, 0.0], [1.0, 0.0], [1.0, 1.0], [0.0, -1.0]])
+    upg = np.array([[2.0, 0.0], [5.0, 0.0], [1.0, -1.0], [0.0, 2.0]])
+    y, n = O.ffn_sparse_zero_skip(x, upg, gate, down, "reglu", allon)
+    assert n == 2 and np.array_equal(y, [5 * 2 - 3 * 3, 5 * 6 - 3 * 7])
+    # SwiGLU is zero only where g = 0 or u = 0: g = (0, 1, 3, -2) -> h_0 = 0
+    gate0 = np.array([[0.0, 0.0], [1.0, 0.0], [1.0, 1.0], [0.0, -1.0]])
+    _, n = O.ffn_sparse_zero_skip(x, upg, gate0, down, "swiglu", allon)
+    assert n == 3
+
+
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
+def test_zero_skip_equals_full_and_library(act):
+    """Skipping the down columns of zero activations leaves y as the library
+    dense FFN over the active neurons gives it, and the number of columns
+    read is the library's count of non-zero activations among them."""
+    rng = np.random.default_rng(300)
+    d, f = 8, 64
+    up, gate, down = _rand_layer(rng, d, f, act)
+    perm = rng.permutation(f)
+    for trial in range(200):
+        x = rng.standard_normal(d)
+        act_slots = rng.random(f) < rng.random()
+        y, n = O.ffn_sparse_zero_skip(x, up, gate, down, act, act_slots, perm)
+        keep = np.zeros(f, dtype=bool)
+        keep[perm[act_slots]] = True
+        upz = up * keep[:, None]
+        gz = gate * keep[:, None] if gate is not None else None
+        assert np.allclose(y, _torch_dense(x, upz, gz, down * keep[None, :], act), rtol=1e-12, atol=1e-12), trial
+        ident = np.eye(f)
+        h = _torch_dense(x, upz, gz, ident, act)      # down = identity: the library's h in original order
+        assert n == int(np.count_nonzero(h[keep])), trial
+
+
 def test_brute_force_scalar_predictor_d8():
     """Each a_i against a scalar recomputation in plain python floats."""
     rng = np.random.default_rng(3)
