@@ -524,3 +524,53 @@ def test_q4_range_and_arithmetic():
     bad[0, 0] = 8
     with pytest.raises(ValueError):
         O.ffn_sparse_q4(x, bad, s_up, None, None, down_q, s_dn, "relu", act)
+
+
+# ---------------------------------------------------------------- stored weights and the dense form
+
+def _store(w, dtype):
+    """Round float64 weights to the stored type with torch (round to nearest
+    even) and return (stored array as the oracle takes it, torch's own widened
+    float64 values of the stored weights)."""
+    t = torch.from_numpy(w)
+    if dtype == "f32":
+        s = t.float()
+        return s.numpy(), s.double().numpy()
+    if dtype == "f16":
+        s = t.half()
+        return s.numpy(), s.double().numpy()
+    s = t.to(torch.bfloat16)
+    return s.view(torch.int16).numpy().view(np.uint16), s.double().numpy()
+
+
+@pytest.mark.parametrize("dtype,act", [("f32", "relu"), ("f16", "swiglu"), ("bf16", "reglu"), ("bf16", "relu2")])
+def test_stored_weights_equal_library_on_torch_widened_values(dtype, act):
+    """The stored-weight form reads only active rows and columns, widens them
+    and applies the definition; it must equal a library dense FFN on torch's
+    own widening of the same stored weights, with the inactive neurons zeroed
+    through the neuron table."""
+    rng = np.random.default_rng(21)
+    d, f = 16, 64
+    up, gate, down = _rand_layer(rng, d, f, act)
+    up_s, up_w = _store(up, dtype)
+    gate_s, gate_w = _store(gate, dtype) if gate is not None else (None, None)
+    down_s, down_w = _store(down, dtype)
+    perm = rng.permutation(f)
+    for trial in range(20):
+        x = rng.standard_normal(d)
+        act_slots = rng.random(f) < 0.3
+        y, _ = O.ffn_sparse_stored(x, up_s, gate_s, down_s, dtype, act, act_slots, perm)
+        keep = np.zeros(f, dtype=bool)
+        keep[perm[act_slots]] = True
+        ref = _torch_dense(x, up_w * keep[:, None], gate_w * keep[:, None] if gate_w is not None else None,
+                           down_w * keep[None, :], act)
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12), trial
+
+
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu", "relu2"])
+def test_dense_form_equals_library(act):
+    rng = np.random.default_rng(22)
+    up, gate, down = _rand_layer(rng, 24, 64, act)
+    x = rng.standard_normal(24)
+    assert np.allclose(O.ffn_dense(x, up, gate, down, act), _torch_dense(x, up, gate, down, act),
+                       rtol=1e-12, atol=1e-12)
