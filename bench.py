@@ -774,7 +774,7 @@ def run_reference(args, world, rank, local):
         oracle_ffn(O, spec, host, x, a, perm)
 
     K = max(1, min(args.steps, args.ref_max_steps))
-    Wm = min(args.warmup, 2)
+    Wm = min(args.warmup, 3)
     for t in range(Wm):
         one(t)
     t0 = time.perf_counter()
