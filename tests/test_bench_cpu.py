@@ -1,0 +1,97 @@
+"""Host logic of the measurement, on CPU.
+
+The bandwidth figures the bench reports are algorithmic bytes divided by
+measured time, so the byte counts are checked here against the per-layer
+figures worked out by hand from each workload's shape: predictor weights
+(W1 is h x d, W2 is f x h, plus one fp32 bias per neuron where the workload
+places activity with b2), plus every FFN row of each active neuron (up, gate
+for the gated activations, and the transposed down row), plus x and y. The
+DRAM-traffic figure is a stored ncu capture scaled by the active rows; the
+bench reports none once the kernel's sources no longer match the capture.
+"""
+
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from activation_sparse_ffn_gb300 import workload as W  # noqa: E402
+
+
+@pytest.mark.parametrize("name,count,pred_bytes,row_bytes,with_b2", [
+    # d 512, f 2048, h 64, fp32, ReLU, ~205 active: W1 64*512*4 + W2 2048*64*4 + b2 2048*4; 205 x 2 rows of 2 KB
+    ("relu_d512_f2048_fp32", 205, 131072 + 524288 + 8192, 205 * 2 * 2048, True),
+    # d 4096, f 16384, h 1024, fp16, ReLU, ~1311 active: 8.4 MB + 33.6 MB; 1311 x 2 rows of 8 KB
+    ("opt6.7b_relu_d4096_f16384_fp16", 1311, 8388608 + 33554432, 1311 * 2 * 8192, False),
+    # d 8192, f 28672, h 1024, bf16, ReGLU, ~2867 active: 16.8 MB + 58.7 MB; 2867 x 3 rows of 16 KB
+    ("llama2_70b_reglu_d8192_f28672_bf16_8l", 2867, 16777216 + 58720256, 2867 * 3 * 16384, False),
+    # d 4096, f 11008, h 512, bf16, SwiGLU, ~5504 active: 4.2 MB + 11.3 MB; 5504 x 3 rows of 8 KB
+    ("swiglu7b_d4096_f11008_bf16_32l", 5504, 4194304 + 11272192, 5504 * 3 * 8192, False),
+])
+def test_layer_bytes_match_the_shapes(name, count, pred_bytes, row_bytes, with_b2):
+    spec = W.WORKLOADS[name]
+    b = bench.layer_bytes(spec, count, with_b2)
+    assert b["metric"] == pred_bytes + row_bytes + 2 * spec.d * 4
+    k = b["kernels"]
+    # the FFN kernel's share: the rows plus x and the mask words
+    assert k["ffn"] == row_bytes + spec.d * 4 + spec.f // 8
+    assert k["pred_hidden"] + k["pred_scores"] >= pred_bytes
+
+
+def test_zero_skip_counts_only_the_down_rows_read():
+    spec = W.WORKLOADS["llama2_70b_reglu_d8192_f28672_bf16_8l"]
+    full = bench.layer_bytes(spec, 1000, False)
+    half = bench.layer_bytes(spec, 1000, False, kept=500)
+    row = spec.d * spec.wbytes
+    assert full["metric"] - half["metric"] == 500 * row
+    assert bench.layer_bytes(spec, 1000, False, kept=1000)["metric"] == full["metric"]
+
+
+def test_quantized_rows_count_codes_and_scales():
+    q8 = W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q8_8l"]
+    q4 = W.WORKLOADS["llama2_70b_reglu_d8192_f28672_q4_8l"]
+    bf = W.WORKLOADS["llama2_70b_reglu_d8192_f28672_bf16_8l"]
+    n = 100
+    pred = bench.layer_bytes(bf, 0, False)["metric"]
+    assert bench.layer_bytes(q8, n, False)["metric"] - pred == n * 3 * (8192 + 4)
+    assert bench.layer_bytes(q4, n, False)["metric"] - pred == n * 3 * (4096 + 4)
+
+
+def test_batch_cost_at_one_token_equals_the_single_token_metric():
+    spec = W.WORKLOADS["falcon40b_relu_d8192_f32768_fp16_batch"]
+    for u in (0, 1, 2294, 13107):
+        assert bench.batch_layer_cost(spec, u, 1, False)["metric"] == bench.layer_bytes(spec, u, False)["metric"]
+    # every extra token adds only its x and y
+    assert (bench.batch_layer_cost(spec, 500, 32, False)["metric"]
+            - bench.batch_layer_cost(spec, 500, 1, False)["metric"]) == 31 * 2 * spec.d * 4
+
+
+def _write_capture(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel source v1\n")
+    d = {
+        "launches": [{"active_neurons": 1000, "dram_read": 48_000_000 + 16_000_000, "dram_write": 1_000_000}],
+        "l2_prefetch_bytes_per_launch": 16_000_000,
+        "sources": [str(src)],
+    }
+    d["sources_sha256"] = bench.sources_sha256(d["sources"])      # absolute paths join to themselves
+    cap = tmp_path / "cap.json"
+    cap.write_text(json.dumps(d))
+    return src, cap
+
+
+def test_traffic_scales_by_active_rows_and_vanishes_when_sources_change(tmp_path, monkeypatch):
+    src, cap = _write_capture(tmp_path)
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "ffn", str(cap))
+    # 49 KB per neuron once the 16 MB prefetch is taken out; the prefetch is added back when on
+    assert bench.measured_traffic("ffn", 2000, prefetch=False) == pytest.approx(2000 * 49_000)
+    assert bench.measured_traffic("ffn", 2000, prefetch=True) == pytest.approx(2000 * 49_000 + 16_000_000)
+    src.write_text("kernel source v2\n")
+    assert bench.measured_traffic("ffn", 2000, prefetch=True) is None
+    assert bench.measured_traffic("no_such_kernel", 2000, prefetch=True) is None
+
