@@ -115,16 +115,20 @@ def sources_sha256(paths) -> str:
     return h.hexdigest()
 
 
-def measured_traffic(kernel: str, units_per_launch: float, prefetch: bool):
+def measured_traffic(kernel: str, units_per_launch: float, prefetch: bool, workload: str):
     """DRAM bytes (read + write) per launch of `kernel` at `units_per_launch`
     active neurons, scaled from the stored capture by units processed (the
     kernel's traffic grows with the active rows it streams), plus the
-    next-layer W1 prefetch when the L2 hint is on; or None."""
+    next-layer W1 prefetch when the L2 hint is on; or None. Bytes per neuron
+    depend on the row length and storage, so a capture only serves the
+    workload it was taken on."""
     rel = TRAFFIC_FILES.get(kernel)
     if rel is None or not os.path.exists(os.path.join(ROOT, rel)):
         return None
     with open(os.path.join(ROOT, rel)) as fh:
         d = json.load(fh)
+    if d.get("bench_workload") != workload:
+        return None   # captured on another layer shape or row format
     if sources_sha256(d["sources"]) != d["sources_sha256"]:
         return None   # the kernel changed since the counters were taken
     l0 = d["launches"][0]
@@ -634,7 +638,7 @@ def run_ours(args, world, rank, local):
     pk = per_kernel[dom]
     dom_traffic = None
     if Bt == 1 and not zero_skip:  # the stored counters are of the kernel without zero-skip
-        t = measured_traffic(dom, float(counts.mean()), prefetch_next)
+        t = measured_traffic(dom, float(counts.mean()), prefetch_next, spec.name)
         dom_traffic = round(t) if t is not None else None
     active_frac = float(tok_counts.mean() / Bt / spec.f)
     line = {

@@ -77,6 +77,7 @@ def _write_capture(tmp_path):
     d = {
         "launches": [{"active_neurons": 1000, "dram_read": 48_000_000 + 16_000_000, "dram_write": 1_000_000}],
         "l2_prefetch_bytes_per_launch": 16_000_000,
+        "bench_workload": "some_layer",
         "sources": [str(src)],
     }
     d["sources_sha256"] = bench.sources_sha256(d["sources"])      # absolute paths join to themselves
@@ -85,13 +86,15 @@ def _write_capture(tmp_path):
     return src, cap
 
 
-def test_traffic_scales_by_active_rows_and_vanishes_when_sources_change(tmp_path, monkeypatch):
+def test_traffic_scales_by_active_rows_only_for_its_workload_and_sources(tmp_path, monkeypatch):
     src, cap = _write_capture(tmp_path)
     monkeypatch.setitem(bench.TRAFFIC_FILES, "ffn", str(cap))
     # 49 KB per neuron once the 16 MB prefetch is taken out; the prefetch is added back when on
-    assert bench.measured_traffic("ffn", 2000, prefetch=False) == pytest.approx(2000 * 49_000)
-    assert bench.measured_traffic("ffn", 2000, prefetch=True) == pytest.approx(2000 * 49_000 + 16_000_000)
+    assert bench.measured_traffic("ffn", 2000, False, "some_layer") == pytest.approx(2000 * 49_000)
+    assert bench.measured_traffic("ffn", 2000, True, "some_layer") == pytest.approx(2000 * 49_000 + 16_000_000)
+    # bytes per neuron of one layer shape say nothing about another
+    assert bench.measured_traffic("ffn", 2000, True, "another_layer") is None
     src.write_text("kernel source v2\n")
-    assert bench.measured_traffic("ffn", 2000, prefetch=True) is None
-    assert bench.measured_traffic("no_such_kernel", 2000, prefetch=True) is None
+    assert bench.measured_traffic("ffn", 2000, True, "some_layer") is None
+    assert bench.measured_traffic("no_such_kernel", 2000, True, "some_layer") is None
 
