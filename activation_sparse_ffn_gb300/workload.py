@@ -124,6 +124,12 @@ WORKLOADS = {
     "opt6.7b_relu_d4096_f16384_fp16": LayerSpec(
         name="opt6.7b_relu_d4096_f16384_fp16", d=4096, f=16384, h=1024, group_size=32,
         act="relu", wdtype="f16", p_mean=0.08, coverage=(0.20, 0.80), tokens=256, seq="ar1"),
+    # The same layer with consecutive tokens at ~0.98 cosine: rho 0.98 with noise
+    # 0.199 keeps unit variance (0.98^2 + 0.199^2 = 1.0).
+    "opt6.7b_relu_d4096_f16384_fp16_rho098": LayerSpec(
+        name="opt6.7b_relu_d4096_f16384_fp16_rho098", d=4096, f=16384, h=1024, group_size=32,
+        act="relu", wdtype="f16", p_mean=0.08, coverage=(0.20, 0.80), tokens=256, seq="ar1",
+        ar_rho=0.98, ar_noise=0.199),
     # LLaMA2-70B-shaped ReGLU stack, bf16, 8 layers, ~10% active, top 26% -> 80%.
     "llama2_70b_reglu_d8192_f28672_bf16_8l": LayerSpec(
         name="llama2_70b_reglu_d8192_f28672_bf16_8l", d=8192, f=28672, h=1024, group_size=64,
@@ -380,6 +386,12 @@ def make_tokens(d: int, T: int, seed: int = 0, kind: str = "iid", batch: int = 1
     for t in range(1, T):
         x[t] = ar_rho * x[t - 1] + ar_noise * e[t]
     return x
+
+
+def spec_tokens(spec: LayerSpec, T: int, seed: int = 0, batch: int = 1, device="cpu") -> torch.Tensor:
+    """:func:`make_tokens` with the workload's sequence kind and AR(1) coefficients."""
+    return make_tokens(spec.d, T, seed=seed, kind=spec.seq, batch=batch, ar_rho=spec.ar_rho,
+                       ar_noise=spec.ar_noise, device=device)
 
 
 def make_stall_bits(T: int, L: int, seed: int = 0) -> np.ndarray:

@@ -327,7 +327,7 @@ def run_ours(args, world, rank, local):
 
     # ---- buffers
     P = max(1, min(args.tokens, spec.tokens))
-    X = W.make_tokens(spec.d, P, seed=args.seed, kind=spec.seq, batch=Bt, device=dev).contiguous()  # [P,B,d]
+    X = W.spec_tokens(spec, P, seed=args.seed, batch=Bt, device=dev).contiguous()  # [P,B,d]
     gw = (spec.n_groups + 31) // 32
     # group masks of all layers, double-buffered by token parity: the momentum
     # update of token t-1 runs while token t's layers write the other buffer
@@ -765,7 +765,7 @@ def run_reference(args, world, rank, local):
     perm = w["perm"].cpu().numpy()
     b2 = None if w["b2"] is None else w["b2"].double().cpu().numpy()
     del w
-    X = W.make_tokens(spec.d, max(1, min(args.tokens, spec.tokens)), seed=args.seed, kind=spec.seq)[:, 0]
+    X = W.spec_tokens(spec, max(1, min(args.tokens, spec.tokens)), seed=args.seed)[:, 0]
     Xs = X.double().numpy()
     W1 = O.widen(host["W1"], spec.wdtype)
     W2 = O.widen(host["W2"], spec.wdtype)

@@ -21,7 +21,7 @@ def _active_matrix(spec, T, seed=0, d=None):
     if d is not None:
         spec = W.spec_replace(spec, d=d)
     L = W.make_layer(spec, seed=seed, layer=0, with_down=False)
-    X = W.make_tokens(spec.d, T, seed=seed, kind=spec.seq)
+    X = W.spec_tokens(spec, T, seed=seed)
     W1 = O.widen(W.stored_numpy(L["W1"]), spec.wdtype)
     W2 = O.widen(W.stored_numpy(L["W2"]), spec.wdtype)
     b2 = None if L["b2"] is None else L["b2"].numpy().astype(np.float64)
@@ -85,6 +85,31 @@ def test_ar1_tokens_correlated():
     assert abs(var - 0.1936 / (1 - 0.81)) < 0.05
     Xi = W.make_tokens(512, 100, seed=3, kind="iid")[:, 0].double()
     assert abs(torch.nn.functional.cosine_similarity(Xi[1:], Xi[:-1], dim=1).mean().item()) < 0.05
+
+
+def test_ar1_variant_at_098_cosine():
+    spec = W.WORKLOADS["opt6.7b_relu_d4096_f16384_fp16_rho098"]
+    X = W.spec_tokens(spec, 300, seed=3)[:, 0].double()
+    cos = torch.nn.functional.cosine_similarity(X[1:], X[:-1], dim=1).mean().item()
+    assert 0.975 < cos < 0.985       # 0.98 / sqrt(0.98^2 + 0.199^2) ~ 0.980
+    assert abs(X[50:].var().item() - 1.0) < 0.05
+    # the base workload's tokens are unchanged by passing its coefficients explicitly
+    base = W.WORKLOADS["opt6.7b_relu_d4096_f16384_fp16"]
+    assert torch.equal(W.spec_tokens(base, 20, seed=3), W.make_tokens(base.d, 20, seed=3, kind="ar1"))
+
+
+def test_correlated_tokens_keep_their_active_sets():
+    """Consecutive tokens at 0.98 cosine share more of their active set than at
+    0.9, at the same mean active fraction."""
+    def overlap(name):
+        spec, _, A = _active_matrix(W.WORKLOADS[name], 60, d=1024)
+        inter = (A[1:] & A[:-1]).sum(1)
+        union = (A[1:] | A[:-1]).sum(1)
+        return float((inter / np.maximum(union, 1)).mean()), float(A.mean())
+    j09, f09 = overlap("opt6.7b_relu_d4096_f16384_fp16")
+    j98, f98 = overlap("opt6.7b_relu_d4096_f16384_fp16_rho098")
+    assert abs(f98 - f09) < 0.02, (f09, f98)
+    assert j98 > j09 + 0.1, (j09, j98)
 
 
 def test_seed_determinism_and_independence():
