@@ -71,6 +71,16 @@ def test_status_strings(lib):
     (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format=5), False),
     (dict(d=512, f=2048, h=64, group_size=32, act="relu2", wdtype="bf16"), True),
     (dict(d=512, f=2048, h=64, group_size=32, act=4, wdtype="bf16"), False),
+    (dict(d=512, f=2048, h=64, group_size=32, act="reglu", wdtype="f16", ffn_format="q4"), True),
+    (dict(d=528, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format="q4"), False),  # d % 32
+    (dict(d=528, f=2048, h=64, group_size=32, act="relu", wdtype="bf16", ffn_format="q8"), True),   # d % 16 is enough
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="f32", ffn_format="q4"), False),   # fp32 predictor
+    (dict(d=16384, f=2048, h=64, group_size=32, act="relu", wdtype="bf16"), True),    # 32 KB rows
+    (dict(d=16392, f=2048, h=64, group_size=32, act="relu", wdtype="f16"), False),    # d > 16384
+    (dict(d=512, f=32, h=64, group_size=64, act="relu", wdtype="f32"), False),        # f < G
+    (dict(d=512, f=65536, h=64, group_size=64, act="relu", wdtype="f16"), True),      # exactly 1024 groups
+    (dict(d=512, f=2048, h=64, group_size=32, act="relu", wdtype="f32", max_batch=0), False),
+    (dict(d=512, f=2048, h=512, group_size=32, act="relu", wdtype="f32"), True),      # 2 KB predictor rows
 ])
 def test_validate(lib, kw, ok):
     desc = lib.make_desc(**kw)
