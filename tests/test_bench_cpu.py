@@ -8,6 +8,8 @@ places activity with b2), plus every FFN row of each active neuron (up, gate
 for the gated activations, and the transposed down row), plus x and y. The
 DRAM-traffic figure is a stored ncu capture scaled by the active rows; the
 bench reports none once the kernel's sources no longer match the capture.
+The clock summary is read from nvidia-smi samples; a fake sample file stands
+in for them here.
 """
 
 import json
@@ -98,3 +100,41 @@ def test_traffic_scales_by_active_rows_only_for_its_workload_and_sources(tmp_pat
     assert bench.measured_traffic("ffn", 2000, True, "some_layer") is None
     assert bench.measured_traffic("no_such_kernel", 2000, True, "some_layer") is None
 
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler_with(tmp_path, rows):
+    path = tmp_path / "clocks.csv"
+    path.write_text("".join(", ".join(r) + "\n" for r in rows))
+    s = bench.ClockSampler(0)
+    s.proc, s.path, s.fh = _DoneProc(), str(path), open(path, "a")
+    return s
+
+
+def _row(sm, util, hw="Not Active", sw_power="Not Active"):
+    # timestamp, index, clocks.sm, clocks.max.sm, power.draw, utilization.gpu, active mask,
+    # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    return ["2026/01/01 00:00:00.000", "0", str(sm), "2070", "650.5", str(util), "0x0", hw,
+            "Not Active", "Not Active", sw_power]
+
+
+def test_clock_summary_uses_busy_samples_and_names_throttle_reasons(tmp_path):
+    rows = [_row(1980, 0), _row(2070, 97), _row(2055, 99), _row(2040, 98, sw_power="Active"), _row(900, 5)]
+    out = _sampler_with(tmp_path, rows).stop()
+    assert out["sm_mhz"] == 2055 and out["sm_max_mhz"] == 2070 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    # a slowdown during the timed region is reported by name
+    out = _sampler_with(tmp_path, [_row(1500, 99, hw="Active"), _row(1490, 99)]).stop()
+    assert out["reasons"] == ["hw_slowdown"] and out["sm_mhz"] == 1495
+
+
+def test_clock_summary_without_nvidia_smi():
+    out = bench.ClockSampler(0).stop()
+    assert out["samples"] == 0 and out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
