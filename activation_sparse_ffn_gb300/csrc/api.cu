@@ -421,14 +421,19 @@ sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const s
   return SFFN_OK;
 }
 
-sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, float thres, const sffn_masks* m,
-                             float* y, float* x_out, void* ws, size_t ws_bytes, sffn_stream stream) {
+static sffn_status check_step(const sffn_layer* L, const float* x, int B, const sffn_masks* m, float* y,
+                              float* x_out, const void* ws, size_t ws_bytes) {
   sffn_status rc = check_hot(L, x, B, m, ws, ws_bytes);
   if (rc != SFFN_OK) return rc;
   if (!y || !aligned(y, 16)) return invalid("y must be a non-NULL 16-byte aligned device pointer");
   if (y == x) return invalid("y must not alias x");
   if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
-  cudaStream_t st = (cudaStream_t)stream;
+  return SFFN_OK;
+}
+
+// predict + forward of one layer (arguments already checked)
+static sffn_status decode_step_launch(const sffn_layer* L, const float* x, int32_t B, float thres,
+                                      const sffn_masks* m, float* y, float* x_out, void* ws, cudaStream_t st) {
   if (B > 1) {
     cudaError_t e = launch_batch(*L, x, B, thres, m, true, true, y, x_out, ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
@@ -447,6 +452,47 @@ sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, flo
     });
   if (e == cudaSuccess) e = traced(*L, 3, st, [&] { return launch_ffn_reduce(*L, part, kept, x, y, x_out, st); });
   if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_decode_step(const sffn_layer* L, const float* x, int32_t B, float thres, const sffn_masks* m,
+                             float* y, float* x_out, void* ws, size_t ws_bytes, sffn_stream stream) {
+  sffn_status rc = check_step(L, x, B, m, y, x_out, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  return decode_step_launch(L, x, B, thres, m, y, x_out, ws, (cudaStream_t)stream);
+}
+
+static sffn_status check_tam_args(const tam_state* S, int32_t layer0, int32_t n_layers, float lambda, float eps,
+                                  int32_t K) {
+  if (!S) return invalid("tam is NULL");
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > S->n_layers) return invalid("layer range out of bounds");
+  if (!(lambda < 1.f) || std::isnan(lambda)) return invalid("lambda must be < 1 (negative: use the state's lambda)");
+  if (!(eps >= 0.f) || std::isinf(eps)) return invalid("eps must be finite and >= 0");
+  if (K < 0 || K > S->n_groups) return invalid("capacity_k must be in [0, n_groups]");
+  return SFFN_OK;
+}
+
+sffn_status sffn_decode_step_tam(const sffn_layer* L, tam_state* S, int32_t layer, const float* x, int32_t B,
+                                 float thres, const sffn_masks* m, float* y, float* x_out, void* ws, size_t ws_bytes,
+                                 float lambda, float eps, int32_t K, const tam_outputs* out, sffn_stream stream) {
+  sffn_status rc = check_step(L, x, B, m, y, x_out, ws, ws_bytes);
+  if (rc != SFFN_OK) return rc;
+  rc = check_tam_args(S, layer, 1, lambda, eps, K);
+  if (rc != SFFN_OK) return rc;
+  if (S->n_groups != L->n_groups) return invalid("the momentum state's group count differs from the layer's");
+  if (S->device != L->device) return invalid("the momentum state lives on another device");
+  // the momentum step reads the token's group bitmask (B = 1) or the batch union's
+  uint32_t* gm = B == 1 ? m->gmask : m->ugmask;
+  if (!gm || !aligned(gm, 4))
+    return invalid(B == 1 ? "masks->gmask is required (the momentum step reads it)"
+                          : "masks->ugmask is required (the momentum step reads the union group bitmask)");
+  cudaStream_t st = (cudaStream_t)stream;
+  rc = decode_step_launch(L, x, B, thres, m, y, x_out, ws, st);
+  if (rc != SFFN_OK) return rc;
+  tam_outputs o = {};
+  if (out) o = *out;
+  cudaError_t e = launch_tam_update(*S, layer, 1, gm, L->gwords, lambda, eps, K, o, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step_tam: launch");
   return SFFN_OK;
 }
 
@@ -491,14 +537,11 @@ sffn_status tam_create(int32_t n_layers, int32_t n_groups, float lambda0, tam_st
 
 sffn_status tam_update(tam_state* S, int32_t layer0, int32_t n_layers, const uint32_t* gmask, int32_t gstride,
                        float lambda, float eps, int32_t K, const tam_outputs* out, sffn_stream stream) {
-  if (!S) return invalid("tam is NULL");
-  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > S->n_layers) return invalid("layer range out of bounds");
+  sffn_status rc = check_tam_args(S, layer0, n_layers, lambda, eps, K);
+  if (rc != SFFN_OK) return rc;
   if (!gmask || !aligned(gmask, 4)) return invalid("gmask must be a non-NULL 4-byte aligned device pointer");
   if (gstride < S->gwords) return invalid("gmask_stride is shorter than a group bitset");
-  if (!(lambda < 1.f) || std::isnan(lambda)) return invalid("lambda must be < 1 (negative: use the state's lambda)");
-  if (!(eps >= 0.f) || std::isinf(eps)) return invalid("eps must be finite and >= 0");
-  if (K < 0 || K > S->n_groups) return invalid("capacity_k must be in [0, n_groups]");
-  sffn_status rc = check_device(S->device);
+  rc = check_device(S->device);
   if (rc != SFFN_OK) return rc;
   tam_outputs o = {};
   if (out) o = *out;

@@ -102,6 +102,8 @@ _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
 _sig("sffn_forward", _c, _vp, _vp, _i32, _P(MasksC), _vp, _vp, _vp, _size, _vp)
 _sig("sffn_decode_step", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp, _size, _vp)
 _sig("sffn_decode_step_static_ws", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp)
+_sig("sffn_decode_step_tam", _c, _vp, _vp, _i32, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp, _size, _f32, _f32, _i32,
+     _P(TamOutputsC), _vp)
 _sig("tam_create", _c, _i32, _i32, _f32, _P(_vp))
 _sig("tam_update", _c, _vp, _i32, _i32, _vp, _i32, _f32, _f32, _i32, _P(TamOutputsC), _vp)
 _sig("tam_adapt", _c, _vp, _i32, _i32, _vp, _f32, _f32, _f32, _vp)
@@ -118,7 +120,7 @@ EXPORTS = [
     "sffn_layer_set_l2_resident", "sffn_layer_set_zero_skip",
     "sffn_layer_pack_q8", "sffn_layer_pack_q4",
     "sffn_layer_check_error",
-    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "tam_create", "tam_update",
+    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "sffn_decode_step_tam", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
     "sffn_selftest_wait_timeout",
 ]
@@ -290,6 +292,15 @@ def sffn_decode_step_static_ws(layer, x, B, thres, masks: "Masks", y, x_out, str
     device memory. Calls sharing a device must not overlap on the GPU."""
     _check(_lib.sffn_decode_step_static_ws(layer, _ptr(x), B, thres, ctypes.byref(masks.c), _ptr(y), _ptr(x_out),
                                            _stream(stream)), "sffn_decode_step_static_ws")
+
+
+def sffn_decode_step_tam(layer, tam, layer_index, x, B, thres, masks: "Masks", y, x_out, ws, lam, eps, capacity_k,
+                         outputs: "TamOutputs | None", stream=None) -> None:
+    """sffn_decode_step, then the momentum step of layer ``layer_index`` on the group bitmask it wrote."""
+    oc = outputs.c if outputs is not None else TamOutputsC()
+    _check(_lib.sffn_decode_step_tam(layer, tam, layer_index, _ptr(x), B, thres, ctypes.byref(masks.c), _ptr(y),
+                                     _ptr(x_out), _ptr(ws), ws.numel() * ws.element_size(), lam, eps, capacity_k,
+                                     ctypes.byref(oc), _stream(stream)), "sffn_decode_step_tam")
 
 
 def sffn_selftest_wait_timeout(layer, limit_us: int, stream=None) -> None:

@@ -66,7 +66,18 @@ def parse_args():
                         "zero-skip); the byte counts then count the rows read")
     p.add_argument("--no-prefetch-next", action="store_true",
                    help="do not let each layer prefetch the next layer's predictor weights into L2")
-    p.add_argument("--ref-max-steps", type=int, default=24)
+    p.add_argument("--normalize", action="store_true",
+                   help="harness stand-in for the rest of a transformer block: each layer is fed x_l / rms(x_l) "
+                        "(torch ops between the layers, outside the library) and the residual stream is "
+                        "x_{l+1} = x_l + y_l; needed to run a deep gated stack without overflow")
+    p.add_argument("--e2e-eager-steps", type=int, default=100,
+                   help="steps of the end-to-end run without CUDA graphs (per-layer C ABI calls)")
+    p.add_argument("--cpu1-seconds", type=float, default=15.0,
+                   help="seconds of the single-thread oracle baseline (0 = skip)")
+    p.add_argument("--ref-budget-s", type=float, default=240.0,
+                   help="reference arm: seconds its warm-up and timed steps may take; beyond it fewer steps are "
+                        "timed and the line says so")
+    p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -253,6 +264,77 @@ def layer_bytes(spec, count: int, with_b2: bool, kept: int | None = None) -> dic
     return {"kernels": k, "metric": metric}
 
 
+L2_BYTES = 126e6   # GB300 L2 (a little below the marketed 129 MB once reserved lines are counted)
+
+
+def stack_bytes(spec, n_layers: int) -> tuple[float, float]:
+    """(weights held by the stack, bytes a token is expected to read): per
+    layer the predictor plus every FFN row, and the predictor plus the rows
+    of p_mean * f active neurons."""
+    d, f, h, wb = spec.d, spec.f, spec.h, spec.wbytes
+    pred = h * d * wb + f * h * wb + (f * 4 if spec.bias_mode else 0)
+    row = int(d * spec.fbytes) + (4 if spec.ffn_quant else 0)
+    held = n_layers * (pred + f * spec.n_mats * row)
+    read = n_layers * (pred + spec.p_mean * f * spec.n_mats * row)
+    return held, read
+
+
+def bench_config(spec, batch: int, n_layers: int, distinct: int, normalize: bool, zero_skip: bool, world: int,
+                 replicas_note: str | None) -> dict:
+    """The workload part of the line's config: identical for both arms."""
+    held, read = stack_bytes(spec, n_layers)
+    if read > L2_BYTES:
+        l2 = (f"inputs larger than L2: the stack holds {held / 1e9:.2f} GB of weights and a token reads about "
+              f"{read / 1e6:.0f} MB of distinct weights (predictors and active rows of every layer)")
+    else:
+        l2 = (f"L2-resident correctness workload: a token reads about {read / 1e6:.1f} MB of weights, less than "
+              f"L2 holds")
+    cfg = {
+        "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": n_layers, "batch": batch,
+        "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype,
+        "ffn_rows": "q4" if spec.ffn_q4 else "q8" if spec.ffn_q8 else spec.wdtype, "thres": spec.thres,
+        "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": spec.capacity,
+                "adaptive_lambda": bool(spec.anb)},
+        "distinct_tokens": distinct,
+        "normalize": ("each layer is fed x_l / rms(x_l), a harness stand-in for the rest of the block (torch ops "
+                      "outside the library); residual x_{l+1} = x_l + y_l") if normalize else None,
+        "zero_skip": zero_skip,
+        "l2": l2,
+        "parallelism": "replicas" if world > 1 else "single",
+    }
+    if replicas_note:
+        cfg["replicas"] = replicas_note
+    return cfg
+
+
+def stack_layers(spec, args) -> tuple[object, str | None]:
+    """The stack the step runs: the workload's layers, or --layers, and a
+    single-layer workload rotated over 4 replicas (so L2 never holds a step's
+    rows). Returns (spec with that layer count, note or None)."""
+    from activation_sparse_ffn_gb300 import workload as W
+    if args.layers:
+        return W.spec_replace(spec, layers=args.layers), None
+    if spec.layers == 1:
+        return (W.spec_replace(spec, layers=4),
+                "single-layer workload rotated over 4 independent layer replicas")
+    return spec, None
+
+
+def rms_normalize(x):
+    """x / rms(x) over the last axis (no learned scale): the harness stand-in
+    for the normalisation a transformer block applies before its FFN."""
+    import torch
+    return x * torch.rsqrt((x * x).mean(dim=-1, keepdim=True))
+
+
+def percentiles_ms(durs: list[float]) -> dict:
+    import numpy as np
+    a = np.asarray(durs, dtype=np.float64)
+    return {"p10": round(float(np.percentile(a, 10)), 5), "p50": round(float(np.percentile(a, 50)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5), "min": round(float(a.min()), 5),
+            "max": round(float(a.max()), 5), "n": int(a.size)}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, world, rank, local):
@@ -273,15 +355,11 @@ def run_ours(args, world, rank, local):
     from activation_sparse_ffn_gb300 import sffn
     from activation_sparse_ffn_gb300 import workload as W
 
-    spec = W.WORKLOADS[args.workload]
+    spec, replicas_note = stack_layers(W.WORKLOADS[args.workload], args)
     Bt = max(1, args.batch)
-    replicas_note = None
-    if args.layers:
-        spec = W.spec_replace(spec, layers=args.layers)
-    elif spec.layers == 1:
-        # a single layer is rotated over 4 replicas so that L2 never holds a step's rows
-        spec = W.spec_replace(spec, layers=4)
-        replicas_note = "single-layer workload rotated over 4 independent layer replicas"
+    normalize = bool(args.normalize)
+    if normalize and (args.lookahead or args.l2_resident_mb):
+        raise SystemExit("--normalize runs the exact method without look-ahead or L2 residency")
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
     nL = spec.layers
@@ -378,6 +456,15 @@ def run_ours(args, world, rank, local):
         predicted from its own input, layer l + 1 from x_l on `pstream` while
         layer l's FFN runs (sffn_forward). `saved` collects each layer's input."""
         outb = (xa, xb)
+        if normalize:
+            resid = x
+            for l in range(nL):
+                xn = rms_normalize(resid)
+                if saved is not None:
+                    saved.append(xn.clone())
+                sffn.sffn_decode_step(layers[l].handle, xn, Bt, spec.thres, masks[l], ybuf, None, ws, stream)
+                resid = resid + ybuf
+            return resid
         if lookahead:
             sffn.sffn_predict(layers[0].handle, x, 1, spec.thres, masks[0], ws_pred, stream)
         for l in range(nL):
@@ -489,21 +576,24 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event after every step (graph launches are serialised anyway, so the
+    # events cost nothing measurable): the total and the per-step percentiles
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t_start = args.warmup
     with torch.cuda.stream(stream):
-        ev0.record(stream)
+        evs[0].record(stream)
         for i in range(args.steps):
             run(t_start + i)
-        ev1.record(stream)
+            evs[i + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_ms, value = replica_job_rate(ev0.elapsed_time(ev1), Bt * args.steps, world, dev)
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    elapsed_ms, value = replica_job_rate(evs[0].elapsed_time(evs[-1]), Bt * args.steps, world, dev)
     for L in layers:
         L.check_error(stream)
     sffn.tam_check_error(tam.handle, stream)
@@ -611,28 +701,62 @@ def run_ours(args, world, rank, local):
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g_e2e, stream=stream):
                 xfin = step(0, xin=xin)
-    E = min(args.e2e_steps, args.steps)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(E):
-            t = (t_start + i) % P
-            xin.copy_(Xh[t], non_blocking=True)
-            if g_e2e is not None:
-                g_e2e.replay()
-                out = xfin
-            else:
-                out = step(t, xin=xin)
-            yh.copy_(out, non_blocking=True)
-            stream.synchronize()
-    e2e_sec = time.perf_counter() - t0
-    e2e_value = world * Bt * E / e2e_sec
+    def e2e_run(n, graph):
+        """n tokens: pinned host x -> device, the step, y -> pinned host, one
+        synchronisation per token. Returns (seconds, per-token ms)."""
+        per = []
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                ti = time.perf_counter()
+                t = (t_start + i) % P
+                xin.copy_(Xh[t], non_blocking=True)
+                if graph is not None:
+                    graph.replay()
+                    out = xfin
+                else:
+                    out = step(t, xin=xin)
+                yh.copy_(out, non_blocking=True)
+                stream.synchronize()
+                per.append(1e3 * (time.perf_counter() - ti))
+        return time.perf_counter() - t0, per
 
-    # ---- CPU baseline: the oracle on layer 0, as it stands
-    cpu = None
+    E = min(args.e2e_steps, args.steps)
+    e2e_sec, e2e_per = e2e_run(E, g_e2e)
+    e2e_value = world * Bt * E / e2e_sec
+    # the same without graphs: every layer's C ABI call issued from Python per token
+    Ee = min(args.e2e_eager_steps, args.steps)
+    e2e_eager = None
+    if Ee > 0:
+        e2e_run(min(3, Ee), None)
+        eager_sec, eager_per = e2e_run(Ee, None)
+        e2e_eager = {"value": round(world * Bt * Ee / eager_sec, 2), "unit": "tokens/s", "steps": Ee,
+                     "ms_per_step": percentiles_ms(eager_per),
+                     "note": "no CUDA graph: each token issues every layer's sffn_decode_step (and the momentum "
+                             "calls) through ctypes, host x in, host y out, one sync per token"}
+
+    # ---- harness cost (the --normalize stand-in alone, same count per step)
+    harness_us = 0.0
+    if normalize:
+        with torch.cuda.stream(stream):
+            hx = X[0].clone()
+            e0.record(stream)
+            for i in range(nd * nL):
+                hx = rms_normalize(hx) + ybuf
+            e1.record(stream)
+        torch.cuda.synchronize()
+        harness_us = 1e3 * e0.elapsed_time(e1) / (nd * nL)
+
+    # ---- CPU baselines: the oracle on layer 0, as it stands (all host
+    # cores through BLAS, and one thread in a separate process)
+    cpu = cpu1 = None
     if want_cpu and host0 is not None:
-        cpu = cpu_baseline(spec, host0, X[:, 0].double().cpu().numpy(), args.cpu_seconds)
+        Xs = X[:, 0].double().cpu().numpy()
+        cpu = cpu_baseline(spec, host0, Xs, args.cpu_seconds)
         cpu["sample"] += "; one token at a time (a batch costs its tokens' sum)" if Bt > 1 else ""
+        if args.cpu1_seconds > 0:
+            cpu1 = cpu_baseline_single_thread(spec, host0, Xs, args.cpu1_seconds)
 
     peak, peak_kind = measured_peaks()
     pk = per_kernel[dom]
@@ -654,16 +778,13 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {
-            "workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": nL, "batch": Bt,
-            "group_size": spec.group_size, "act": spec.act, "weights": spec.wdtype, "thres": spec.thres,
-            "tam": {"lambda": spec.tam_lambda, "eps": spec.tam_eps, "capacity": K},
-            "distinct_tokens": P, "graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
-            "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
-            "zero_skip": zero_skip,
-            "l2": "inputs larger than L2: each step reads %.2f GB of distinct weights" % (timed_bytes / args.steps / 1e9),
-            "parallelism": "replicas" if world > 1 else "single",
-        },
+        "config": bench_config(spec, Bt, nL, P, normalize, zero_skip, world, replicas_note),
+        "run": {"graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
+                "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
+                "timed_bytes_per_step_gb": round(timed_bytes / args.steps / 1e9, 4),
+                "l2_between_steps": "not flushed: every step reads more distinct weights than L2 holds"
+                                    if stack_bytes(spec, nL)[1] > L2_BYTES else "not flushed (L2-resident workload)"},
+        "ms_per_step_pct": percentiles_ms(step_ms),
         "us_per_layer": round(1e3 * ms_per_step / nL, 3),
         "active_frac": round(active_frac, 5),
         "algorithmic_gbs": round(step_gbs, 1),
@@ -678,20 +799,25 @@ def run_ours(args, world, rank, local):
                      "unit": "GB/s", "frac": round(pk["gbs"] / peak, 4), "traffic": dom_traffic,
                      "peak_kind": peak_kind},
         "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": Bt * spec.d * 4,
-                "d2h_bytes_per_step": Bt * spec.d * 4, "steps": E, "sync_per_step": True},
+                "d2h_bytes_per_step": Bt * spec.d * 4, "steps": E, "sync_per_step": True,
+                "ms_per_step": percentiles_ms(e2e_per),
+                "note": "one CUDA graph per token (all layers and the momentum step) through the library's C ABI"},
+        "e2e_eager": e2e_eager,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
-    if replicas_note:
-        line["config"]["replicas"] = replicas_note
+    if cpu1 is not None:
+        line["cpu_baseline_single_thread"] = cpu1
+    if normalize:
+        line["harness_us_per_layer"] = round(harness_us, 3)
     line["census"] = {"distinct_tokens": P, "active_count_token0_by_layer": [int(c) for c in counts[0]]}
     if zero_skip:
         line["zero_skip"] = {"down_rows_read_frac": round(float(kept.sum() / max(1, counts.sum())), 5),
                              "note": "bytes count the downT rows read (neurons with h != 0), all up/gate rows"}
     if lookahead:
         line["config"]["mode"] = "one-layer-ahead prediction (layer l+1 predicted from layer l's input)"
-        line["config"]["sm_split"] = {"predictor": lookahead, "ffn": n_sms - lookahead}
+        line["run"]["sm_split"] = {"predictor": lookahead, "ffn": n_sms - lookahead}
         line["lookahead"] = {"recall": round(la_hits / max(1, la_exact), 4),
                              "extra_over_exact": round(la_extra / max(1, la_exact), 4),
                              "note": "layers 1.. of every census token; layer 0 is predicted from its own input"}
@@ -747,9 +873,80 @@ def cpu_baseline(spec, host, Xs, seconds):
                       f"(numpy fp64, BLAS threads = available cores), stack time = {spec.layers} x layer time"}
 
 
+def cpu_baseline_single_thread(spec, host, Xs, seconds):
+    """cpu_baseline with one thread: the layer's stored arrays go to a
+    temporary directory and a fresh interpreter, started with every BLAS
+    thread count at 1, times the oracle on them (a child process: the
+    thread count of numpy's BLAS is fixed when it loads)."""
+    import numpy as np
+    with tempfile.TemporaryDirectory(prefix="sffn_cpu1_") as tmp:
+        meta = {"workload": spec.name, "layers": spec.layers, "seconds": seconds, "arrays": []}
+        for k, v in host.items():
+            if isinstance(v, np.ndarray):
+                np.save(os.path.join(tmp, k + ".npy"), v)
+                meta["arrays"].append(k)
+        np.save(os.path.join(tmp, "_X.npy"), Xs)
+        with open(os.path.join(tmp, "meta.json"), "w") as fh:
+            json.dump(meta, fh)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", tmp], capture_output=True,
+                           text=True, env=env, timeout=600 + 4 * seconds)
+        lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        if r.returncode != 0 or not lines:
+            return {"unavailable": f"single-thread worker failed (rc {r.returncode}): {r.stderr[-300:]}"}
+        return json.loads(lines[-1])
+
+
+def cpu_worker(tmp: str) -> None:
+    """Child process of cpu_baseline_single_thread."""
+    import numpy as np
+    from activation_sparse_ffn_gb300 import workload as W
+    with open(os.path.join(tmp, "meta.json")) as fh:
+        meta = json.load(fh)
+    host = {k: np.load(os.path.join(tmp, k + ".npy")) for k in meta["arrays"]}
+    for k in ("b2f", "gate", "gate_q", "gate_s"):
+        host.setdefault(k, None)
+    spec = W.spec_replace(W.WORKLOADS[meta["workload"]], layers=meta["layers"])
+    r = cpu_baseline(spec, host, np.load(os.path.join(tmp, "_X.npy")), meta["seconds"])
+    r["cores"] = 1
+    r["sample"] = r["sample"].replace("BLAS threads = available cores", "one thread: BLAS and OpenMP threads = 1")
+    print(json.dumps(r), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm (the oracle)
 
+def host_layer(W, O, spec, seed, layer, dev):
+    """Stored host copies of one layer, in the form the oracle reads."""
+    import torch
+    w = W.make_layer(spec, seed=seed, layer=layer, device=dev)
+    host = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v) for k, v in w.items()}
+    host["perm"] = w["perm"].cpu().numpy()
+    host["b2f"] = None if w["b2"] is None else w["b2"].double().cpu().numpy()
+    host["W1w"] = O.widen(host["W1"], spec.wdtype)
+    host["W2w"] = O.widen(host["W2"], spec.wdtype)
+    del w
+    return host
+
+
+def oracle_layer(O, spec, host, x):
+    """One layer of the decode step in the oracle: predictor, threshold,
+    mask views, sparse FFN. Returns y."""
+    perm = host["perm"]
+    s = O.predictor_scores(host["W2w"], O.predictor_hidden(host["W1w"], x), host["b2f"])[perm]
+    a = O.active_from_scores(s, spec.thres)
+    O.mask_views(a, spec.group_size)
+    y, _ = oracle_ffn(O, spec, host, x, a, perm)
+    return y
+
+
 def run_reference(args, world, rank, local):
+    """The reference arm: the oracle as it stands on the host cores, on the
+    same workload, stack and token sequence as our arm. One step = one decode
+    token (every token of the batch) through every layer of the stack, the
+    residual x_{l+1} = x_l + y_l (or the --normalize stand-in), as our arm's
+    step. Warm-up steps are all run; the timed steps are all run unless they
+    would exceed --ref-budget-s, in which case the line times fewer and says so."""
     if rank != 0:
         return
     import numpy as np
@@ -758,53 +955,87 @@ def run_reference(args, world, rank, local):
     from activation_sparse_ffn_gb300 import workload as W
     from oracle import sffn_oracle as O
 
-    spec = W.WORKLOADS[args.workload]
+    spec, replicas_note = stack_layers(W.WORKLOADS[args.workload], args)
+    Bt = max(1, args.batch)
+    nL = spec.layers
+    P = max(1, min(args.tokens, spec.tokens))
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = W.make_layer(spec, seed=args.seed, layer=0, device=dev)
-    host = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v) for k, v in w.items()}
-    perm = w["perm"].cpu().numpy()
-    b2 = None if w["b2"] is None else w["b2"].double().cpu().numpy()
-    del w
-    X = W.spec_tokens(spec, max(1, min(args.tokens, spec.tokens)), seed=args.seed)[:, 0]
-    Xs = X.double().numpy()
-    W1 = O.widen(host["W1"], spec.wdtype)
-    W2 = O.widen(host["W2"], spec.wdtype)
+    hosts = [host_layer(W, O, spec, args.seed, l, dev) for l in range(nL)]
+    X = W.spec_tokens(spec, P, seed=args.seed, batch=Bt).double().numpy()     # [P, B, d]
+
+    def rms(v):
+        return v / np.sqrt(np.mean(v * v))
 
     def one(t):
-        x = Xs[t % Xs.shape[0]]
-        s = O.predictor_scores(W2, O.predictor_hidden(W1, x), b2)[perm]
-        a = O.active_from_scores(s, spec.thres)
-        O.mask_views(a, spec.group_size)
-        oracle_ffn(O, spec, host, x, a, perm)
+        for b in range(Bt):
+            x = X[t % P, b]
+            for l in range(nL):
+                xin = rms(x) if args.normalize else x
+                x = x + oracle_layer(O, spec, hosts[l], xin)
 
-    K = max(1, min(args.steps, args.ref_max_steps))
-    Wm = min(args.warmup, 3)
-    for t in range(Wm):
+    t_begin = time.perf_counter()
+    warm = []
+    for t in range(args.warmup):
+        t0 = time.perf_counter()
         one(t)
-    t0 = time.perf_counter()
-    for i in range(K):
-        one(Wm + i)
-    sec = time.perf_counter() - t0
-    per_layer = sec / K
-    value = 1.0 / (spec.layers * per_layer)
+        warm.append(time.perf_counter() - t0)
+    est = (warm[-1] if warm else None)
+    K = max(1, args.steps)
+    if est is None:
+        t0 = time.perf_counter()
+        one(0)
+        est = time.perf_counter() - t0
+    left = args.ref_budget_s - (time.perf_counter() - t_begin)
+    K_run = max(1, min(K, int(left / est)))
+    per = []
+    for i in range(K_run):
+        t0 = time.perf_counter()
+        one(args.warmup + i)
+        per.append(time.perf_counter() - t0)
+    sec = sum(per)
+    value = Bt * K_run / sec
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"each step = the oracle on one layer-token (layer 0 of {spec.layers}); {K} steps "
-              f"(requested {args.steps}); stack time = {spec.layers} x layer time")
+    sample = (f"each step = {Bt} token(s) through all {nL} layers of the stack (oracle: numpy fp64, BLAS threads "
+              f"= available cores); {K_run} timed steps" + (f" of {K} requested (time budget "
+                                                           f"{args.ref_budget_s:.0f} s)" if K_run < K else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": Wm, "ms_per_step": round(1e3 * per_layer * spec.layers, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "d": spec.d, "f": spec.f, "h": spec.h, "layers": spec.layers, "batch": 1},
+        "steps": K_run, "warmup": args.warmup, "ms_per_step": round(1e3 * sec / K_run, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": bench_config(spec, Bt, nL, P, bool(args.normalize), bool(args.zero_skip), world, replicas_note),
+        "ms_per_step_pct": percentiles_ms([1e3 * v for v in per]),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if K_run < K:
+        line["steps_requested"] = K
     print(json.dumps(line), flush=True)
+
+
+def launch_replicas(n: int) -> int:
+    """`bench.py --gpus N` run directly (no WORLD_SIZE): start N replica
+    processes of this command under torch.distributed.run on 127.0.0.1 and
+    return its exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
 
 
 def main():
     args = parse_args()
+    if args.cpu_worker:
+        cpu_worker(args.cpu_worker)
+        return
     world, rank, local = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        raise SystemExit(launch_replicas(args.gpus))
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but the launcher started {world} rank(s)")
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:

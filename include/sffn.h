@@ -311,11 +311,15 @@ sffn_status sffn_decode_step(const sffn_layer* layer, const float* x, int32_t B,
  * loop that must never stall on an allocation (one can synchronize the whole
  * GPU), a runtime that reaches this library only through its C ABI and has no
  * CUDA allocator, or a process whose memory pool refuses new allocations once
- * serving starts. Same arguments and results as sffn_decode_step, minus the
- * workspace: scratch comes from one 16 MiB device array inside the library,
- * which every GPU that loads the library holds until the process exits. It is
- * enough for any valid layer at B = 1 on a GPU with up to about 240 SMs; a
- * layer/batch needing more returns INVALID_ARG. The call allocates nothing. Its first call on each device looks
+ * serving starts. Same arguments and results as sffn_decode_step at B = 1,
+ * minus the workspace: scratch comes from one 16 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. B > 1 returns UNSUPPORTED (the batched path's scratch is not held in
+ * the array). The array is enough for any valid layer at B = 1 on a GPU with
+ * up to about 240 SMs (the per-block partial sums take SMs x d x 4 bytes, at
+ * most 10 MB on a 152-SM GB300, so no valid layer reaches the limit there); a
+ * layer needing more returns INVALID_ARG. The call allocates nothing and
+ * records no sffn_layer_set_trace events. Its first call on each device looks
  * up the array's device address (cudaGetSymbolAddress), so make that first
  * call before any stream capture. All calls on a device share the array:
  * calls that can overlap on the GPU race on it and must be ordered by the
@@ -361,6 +365,25 @@ typedef struct {
 sffn_status tam_update(tam_state* tam, int32_t layer0, int32_t n_layers, const uint32_t* gmask,
                        int32_t gmask_stride, float lambda, float eps, int32_t capacity_k,
                        const tam_outputs* out, sffn_stream stream);
+
+/* The whole per-layer decode step as the pages order it: the predictor, the
+ * sparse FFN on the predicted masks (sffn_decode_step), then one momentum
+ * step of layer `layer_index` of `tam` (tam_update with layer0 = layer_index,
+ * n_layers = 1) on the group bitmask this call writes: masks->gmask for B = 1, the batch
+ * union masks->ugmask for B > 1 (KAIROX 核心方法 item 4: the momentum of every
+ * group is updated at every token from the predicted need; PowerInfer §5.1
+ * for the predictor). All three are enqueued on `stream` in that order. The
+ * momentum arguments mean what they mean for tam_update; `out` may be NULL.
+ * The state must have the layer's group count and live on the same device.
+ * Equivalent to sffn_decode_step followed by tam_update on the same stream;
+ * a caller running many layers may instead batch the momentum steps of all
+ * layers into one tam_update per token on a second stream (same results).
+ * Errors: as sffn_decode_step and tam_update, and INVALID_ARG when the needed
+ * group bitmask pointer is NULL. */
+sffn_status sffn_decode_step_tam(const sffn_layer* layer, tam_state* tam, int32_t layer_index, const float* x,
+                                 int32_t B, float thres, const sffn_masks* masks, float* y, float* x_out,
+                                 void* ws, size_t ws_bytes, float lambda, float eps, int32_t capacity_k,
+                                 const tam_outputs* out, sffn_stream stream);
 
 /* Adaptive Neuron Balancer step (KAIROX 核心方法 item 5) for layers
  * [layer0, layer0 + n_layers): lambda_l <- min(hi, max(lo, lambda_l + (stall[l] ?

@@ -96,6 +96,8 @@ def test_null_handles_are_rejected_on_the_host(lib):
     assert L.sffn_forward(None, None, 1, ctypes.byref(m), None, None, None, 0, None) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_decode_step(None, None, 1, 0.0, ctypes.byref(m), None, None, None, 0, None) == lib.SFFN_ERR_INVALID_ARG
     o = lib.TamOutputsC()
+    assert L.sffn_decode_step_tam(None, None, 0, None, 1, 0.0, ctypes.byref(m), None, None, None, 0, 0.9, 0.01, 1,
+                                  ctypes.byref(o), None) == lib.SFFN_ERR_INVALID_ARG
     assert L.tam_update(None, 0, 1, None, 1, 0.9, 0.01, 1, ctypes.byref(o), None) == lib.SFFN_ERR_INVALID_ARG
     assert L.tam_adapt(None, 0, 1, None, 0.01, 0.8, 0.99, None) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_layer_pack(None, None, None, None, None, None, None, None, None, None) == lib.SFFN_ERR_INVALID_ARG

@@ -69,3 +69,43 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_flag_without_a_launcher_starts_that_many_ranks():
+    """`bench.py --gpus 2` run directly starts two replica processes itself
+    (torch.distributed.run on 127.0.0.1); rank 0 prints the one line with
+    n_gpus 2. A rank count that differs from --gpus is refused."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--workload",
+           "relu_d512_f2048_fp32", "--steps", "2", "--warmup", "1", "--tokens", "2"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env.update(OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas"
+    bad = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT,
+                         env=dict(env, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0"))
+    assert bad.returncode != 0 and "--gpus 2" in bad.stderr
+
+
+def test_reference_arm_times_what_it_prints():
+    """The reference arm runs every warm-up step, times whole tokens through
+    the whole stack, and prints the config keys our arm prints."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from activation_sparse_ffn_gb300 import workload as W
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           "relu_d512_f2048_fp32", "--steps", "3", "--warmup", "2", "--tokens", "4"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env.update(OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["steps"] == 3 and d["warmup"] == 2
+    assert d["value"] == pytest.approx(1e3 / d["ms_per_step"], rel=1e-3)
+    spec = W.spec_replace(W.WORKLOADS["relu_d512_f2048_fp32"], layers=4)
+    want = bench.bench_config(spec, 1, 4, 4, False, False, 1,
+                              "single-layer workload rotated over 4 independent layer replicas")
+    assert d["config"] == json.loads(json.dumps(want))

@@ -50,7 +50,12 @@ def test_static_workspace_matches_caller_workspace():
     L.check_error()
 
 
-def test_static_workspace_rejects_oversized_requests():
+def test_static_workspace_rejects_batches_above_one():
+    """B > 1 is refused with UNSUPPORTED before any device work. The other
+    refusal, a layer whose B = 1 scratch exceeds the 16 MiB array, cannot be
+    reached on a GB300: the scratch is the hidden vector plus one partial sum
+    of y per FFN block, at most 152 x 16384 x 4 bytes (under 10 MB), and
+    sffn_layer_set_grid never raises the block count above the SM count."""
     import __graft_entry__
     __graft_entry__.build()
     from activation_sparse_ffn_gb300 import sffn
@@ -63,4 +68,7 @@ def test_static_workspace_rejects_oversized_requests():
     y = torch.empty(2, 64, device="cuda")
     with pytest.raises(sffn.SffnError) as e:
         sffn.sffn_decode_step_static_ws(L.handle, x, 2, 0.0, L.masks(2), y, None)
-    assert e.value.status in (sffn.SFFN_ERR_UNSUPPORTED, sffn.SFFN_ERR_INVALID_ARG)
+    assert e.value.status == sffn.SFFN_ERR_UNSUPPORTED
+    # the largest valid B = 1 scratch on this GPU fits the array
+    big = sffn.Layer(16384, 64, 8, 32, "relu", "bf16")
+    assert sffn.sffn_workspace_bytes(big.handle, 1) <= 16 << 20
