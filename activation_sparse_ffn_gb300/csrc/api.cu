@@ -611,6 +611,116 @@ void tam_destroy(tam_state* S) {
   delete S;
 }
 
+// ---------------------------------------------------------------- whole-stack decode
+
+sffn_status sffn_stack_create(const sffn_layer* const* layers, int32_t n_layers, sffn_stack** out) {
+  if (!out) return invalid("out is NULL");
+  if (!layers) return invalid("layers is NULL");
+  if (n_layers < 1 || n_layers > 4096) return invalid("n_layers must be in [1, 4096]");
+  const sffn_layer* L0 = layers[0];
+  if (!L0) return invalid("layers[0] is NULL");
+  for (int l = 0; l < n_layers; ++l) {
+    const sffn_layer* L = layers[l];
+    if (!L) return invalid("a layer handle is NULL");
+    const sffn_layer_desc &a = L->desc, &b = L0->desc;
+    if (a.d != b.d || a.f != b.f || a.h != b.h || a.group_size != b.group_size || a.act != b.act ||
+        a.wdtype != b.wdtype || a.ffn_format != b.ffn_format)
+      return invalid("every layer of a stack must have the same shape, activation and storage");
+    if (L->device != L0->device) return invalid("every layer of a stack must live on the same device");
+  }
+  std::string why;
+  if (!stack_supported(*L0, &why)) {
+    set_error(why);
+    return SFFN_ERR_UNSUPPORTED;
+  }
+  sffn_status rc = check_device(L0->device);
+  if (rc != SFFN_OK) return rc;
+  sffn_stack* S = new (std::nothrow) sffn_stack();
+  if (!S) return invalid("host allocation failed");
+  S->n_layers = n_layers;
+  S->device = L0->device;
+  S->layers = new (std::nothrow) const sffn_layer*[n_layers];
+  const size_t one = stack_layer_desc_bytes();
+  unsigned char* table = new (std::nothrow) unsigned char[one * n_layers];
+  if (!S->layers || !table) {
+    delete[] table;
+    sffn_stack_destroy(S);
+    return invalid("host allocation failed");
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    S->layers[l] = layers[l];
+    stack_fill_layer_desc(*layers[l], table + one * l);
+  }
+  cudaError_t e = cudaMalloc(&S->dev_layers, one * n_layers);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&S->bar, 256);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&S->err, 256);
+  if (e == cudaSuccess) e = cudaMemcpy(S->dev_layers, table, one * n_layers, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(S->bar, 0, 256);
+  if (e == cudaSuccess) e = cudaMemset(S->err, 0, 256);
+  if (e == cudaSuccess) e = configure_stack_kernels(*L0);
+  delete[] table;
+  if (e != cudaSuccess) {
+    rc = cuda_fail(e, "sffn_stack_create");
+    sffn_stack_destroy(S);
+    return rc;
+  }
+  *out = S;
+  return SFFN_OK;
+}
+
+size_t sffn_stack_workspace_bytes(const sffn_stack* S) {
+  if (!S) return 0;
+  return stack_ws_bytes(*S->layers[0]);
+}
+
+sffn_status sffn_stack_decode(const sffn_stack* S, const float* x0, float* xs, float* ys, float thres,
+                              const sffn_masks* m, void* ws, size_t ws_bytes, sffn_stream stream) {
+  if (!S) return invalid("stack is NULL");
+  const sffn_layer& L = *S->layers[0];
+  const size_t d = (size_t)L.desc.d, nL = (size_t)S->n_layers;
+  if (!x0 || !aligned(x0, 16)) return invalid("x0 must be a non-NULL 16-byte aligned device pointer");
+  if (!xs || !aligned(xs, 16)) return invalid("xs must be a non-NULL 16-byte aligned device pointer");
+  if (ys && !aligned(ys, 16)) return invalid("ys must be 16-byte aligned");
+  if (!m || !m->nmask || !aligned(m->nmask, 4)) return invalid("masks and masks->nmask are required");
+  // x0 may be one of xs's rows (the previous token's output), or lie apart from xs and ys
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x0), sa = reinterpret_cast<uintptr_t>(xs);
+  const bool in_xs = xa >= sa && xa < sa + nL * d * 4;
+  if (in_xs && (xa - sa) % (d * 4) != 0) return invalid("x0 inside xs must start one of its rows");
+  if (ys) {
+    const uintptr_t ya = reinterpret_cast<uintptr_t>(ys);
+    if ((xa + d * 4 > ya && xa < ya + nL * d * 4) || (sa + nL * d * 4 > ya && sa < ya + nL * d * 4))
+      return invalid("ys must not overlap x0 or xs");
+  }
+  if (!ws) return invalid("ws is NULL");
+  if (!aligned(ws, 256)) return invalid("ws must be 256-byte aligned");
+  if (ws_bytes < stack_ws_bytes(L)) return invalid("ws_bytes is smaller than sffn_stack_workspace_bytes(stack)");
+  sffn_status rc = check_device(S->device);
+  if (rc != SFFN_OK) return rc;
+  cudaError_t e = launch_stack(*S, x0, xs, ys, thres, *m, ws, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "sffn_stack_decode: launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_stack_check_error(const sffn_stack* S, sffn_stream stream) {
+  if (!S) return invalid("stack is NULL");
+  sffn_status rc = read_error_word(S->err, (cudaStream_t)stream);
+  if (rc == SFFN_ERR_TIMEOUT || rc == SFFN_ERR_DEVICE) {
+    // a kernel that wound down may have left the grid barrier half-way
+    cudaError_t e = cudaMemset(S->bar, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "sffn_stack_check_error: reset the grid barrier");
+  }
+  return rc;
+}
+
+void sffn_stack_destroy(sffn_stack* S) {
+  if (!S) return;
+  if (S->dev_layers) cudaFree(S->dev_layers);
+  if (S->bar) cudaFree(S->bar);
+  if (S->err) cudaFree(S->err);
+  delete[] S->layers;
+  delete S;
+}
+
 // ---------------------------------------------------------------- self-test
 
 sffn_status sffn_selftest_wait_timeout(const sffn_layer* L, int32_t limit_us, sffn_stream stream) {

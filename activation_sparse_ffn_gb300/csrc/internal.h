@@ -64,6 +64,17 @@ struct tam_state {
   uint32_t* err = nullptr;
 };
 
+// A stack of layers decoded by one persistent kernel per token
+// (sffn_stack_decode). The layers are not owned.
+struct sffn_stack {
+  int n_layers = 0;
+  int device = 0;
+  const sffn_layer** layers = nullptr;  // host array [n_layers]
+  void* dev_layers = nullptr;           // device table of the layers' packed arrays
+  unsigned* bar = nullptr;              // grid barrier: arrivals, generation
+  uint32_t* err = nullptr;              // device error word
+};
+
 namespace sffn {
 
 // Bytes of one stored FFN row (d weights).
@@ -115,6 +126,15 @@ cudaError_t launch_tam_update(tam_state& S, int layer0, int n_layers, const uint
 cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8_t* stall, float alpha,
                              float lo, float hi, cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint32_t* err, int limit_us, cudaStream_t st);
+
+// Whole-stack decode kernel (stack.cu).
+bool stack_supported(const sffn_layer& L, std::string* why);
+cudaError_t configure_stack_kernels(const sffn_layer& L);
+size_t stack_ws_bytes(const sffn_layer& L);
+size_t stack_layer_desc_bytes();
+void stack_fill_layer_desc(const sffn_layer& L, void* out);
+cudaError_t launch_stack(const sffn_stack& S, const float* x0, float* xs, float* ys, float thres,
+                         const sffn_masks& m, void* ws, cudaStream_t st);
 
 // Packing (setup).
 // up_s, gate_s, down_s: per-neuron scales of SFFN_FFN_Q8 / Q4 rows (original order), else null.

@@ -104,6 +104,11 @@ _sig("sffn_decode_step", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp, _s
 _sig("sffn_decode_step_static_ws", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp)
 _sig("sffn_decode_step_tam", _c, _vp, _vp, _i32, _vp, _i32, _f32, _P(MasksC), _vp, _vp, _vp, _size, _f32, _f32, _i32,
      _P(TamOutputsC), _vp)
+_sig("sffn_stack_create", _c, _P(_vp), _i32, _P(_vp))
+_sig("sffn_stack_workspace_bytes", _size, _vp)
+_sig("sffn_stack_decode", _c, _vp, _vp, _vp, _vp, _f32, _P(MasksC), _vp, _size, _vp)
+_sig("sffn_stack_check_error", _c, _vp, _vp)
+_sig("sffn_stack_destroy", None, _vp)
 _sig("tam_create", _c, _i32, _i32, _f32, _P(_vp))
 _sig("tam_update", _c, _vp, _i32, _i32, _vp, _i32, _f32, _f32, _i32, _P(TamOutputsC), _vp)
 _sig("tam_adapt", _c, _vp, _i32, _i32, _vp, _f32, _f32, _f32, _vp)
@@ -120,7 +125,9 @@ EXPORTS = [
     "sffn_layer_set_l2_resident", "sffn_layer_set_zero_skip",
     "sffn_layer_pack_q8", "sffn_layer_pack_q4",
     "sffn_layer_check_error",
-    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "sffn_decode_step_tam", "tam_create", "tam_update",
+    "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "sffn_decode_step_tam",
+    "sffn_stack_create", "sffn_stack_workspace_bytes", "sffn_stack_decode", "sffn_stack_check_error",
+    "sffn_stack_destroy", "tam_create", "tam_update",
     "tam_adapt", "tam_get_state", "tam_set_state", "tam_get_shape", "tam_check_error", "tam_destroy",
     "sffn_selftest_wait_timeout",
 ]
@@ -307,6 +314,33 @@ def sffn_selftest_wait_timeout(layer, limit_us: int, stream=None) -> None:
     _check(_lib.sffn_selftest_wait_timeout(layer, limit_us, _stream(stream)), "sffn_selftest_wait_timeout")
 
 
+# ----------------------------------------------------------------- whole-stack calls
+
+def sffn_stack_create(layers) -> int:
+    """layers: sequence of layer handles (ints)."""
+    arr = (_vp * len(layers))(*layers)
+    h = _vp()
+    _check(_lib.sffn_stack_create(arr, len(layers), ctypes.byref(h)), "sffn_stack_create")
+    return h.value
+
+
+def sffn_stack_workspace_bytes(stack) -> int:
+    return int(_lib.sffn_stack_workspace_bytes(stack))
+
+
+def sffn_stack_decode(stack, x0, xs, ys, thres, masks: "StackMasks", ws, stream=None) -> None:
+    _check(_lib.sffn_stack_decode(stack, _ptr(x0), _ptr(xs), _ptr(ys), thres, ctypes.byref(masks.c), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)), "sffn_stack_decode")
+
+
+def sffn_stack_check_error(stack, stream=None) -> None:
+    _check(_lib.sffn_stack_check_error(stack, _stream(stream)), "sffn_stack_check_error")
+
+
+def sffn_stack_destroy(stack) -> None:
+    _lib.sffn_stack_destroy(stack)
+
+
 # ----------------------------------------------------------------- TAM calls
 
 def tam_create(n_layers: int, n_groups: int, lambda0: float) -> int:
@@ -369,6 +403,53 @@ class Masks:
         self.ucount = torch.zeros(1, **kw)
         self.c = MasksC(*(t.data_ptr() for t in (self.nmask, self.gmask, self.idx, self.count, self.unmask,
                                                    self.ugmask, self.uidx, self.ucount)))
+
+
+class StackMasks:
+    """Per-layer mask buffers of sffn_stack_decode: nmask [L][f/32], gmask
+    [L][gw], idx [L][f], count [L] (torch int32 on the device)."""
+
+    def __init__(self, n_layers: int, f: int, group_size: int, device="cuda"):
+        n_groups = f // group_size
+        self.nwords, self.gwords = f // 32, (n_groups + 31) // 32
+        kw = dict(dtype=torch.int32, device=device)
+        self.nmask = torch.zeros(n_layers, self.nwords, **kw)
+        self.gmask = torch.zeros(n_layers, self.gwords, **kw)
+        self.idx = torch.full((n_layers, f), -1, **kw)
+        self.count = torch.zeros(n_layers, **kw)
+        self.c = MasksC(self.nmask.data_ptr(), self.gmask.data_ptr(), self.idx.data_ptr(), self.count.data_ptr(),
+                        None, None, None, None)
+
+
+class Stack:
+    """Owns one sffn_stack handle over ``layers`` (Layer objects, kept alive)."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        self.handle = sffn_stack_create([L.handle for L in self.layers])
+        self.n_layers = len(self.layers)
+        L0 = self.layers[0]
+        self.d, self.f, self.group_size = L0.d, L0.f, L0.group_size
+
+    def workspace(self, device="cuda") -> torch.Tensor:
+        return torch.empty(sffn_stack_workspace_bytes(self.handle), dtype=torch.uint8, device=device)
+
+    def masks(self, device="cuda") -> StackMasks:
+        return StackMasks(self.n_layers, self.f, self.group_size, device)
+
+    def check_error(self, stream=None) -> None:
+        sffn_stack_check_error(self.handle, stream)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            sffn_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class TamOutputs:

@@ -77,6 +77,12 @@ def parse_args():
     p.add_argument("--ref-budget-s", type=float, default=240.0,
                    help="reference arm: seconds its warm-up and timed steps may take; beyond it fewer steps are "
                         "timed and the line says so")
+    p.add_argument("--stack", action="store_true",
+                   help="B = 1: run each token through the whole stack in one persistent kernel "
+                        "(sffn_stack_decode) instead of four kernels per layer; the momentum step follows it")
+    p.add_argument("--no-topic-shift", action="store_true",
+                   help="workloads with a topic shift: keep one topic (by default the second half of the cycled "
+                        "tokens runs with every layer's group ranks redrawn)")
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -279,8 +285,18 @@ def stack_bytes(spec, n_layers: int) -> tuple[float, float]:
     return held, read
 
 
+def topic_shift_note(spec, args, distinct: int) -> str | None:
+    """The workload's topic shift, placed inside the cycled token set: tokens
+    [P/2, P) of every P-token cycle run with every layer's group ranks redrawn
+    (a second W2 per layer), so the shift and the shift back are both timed."""
+    if not spec.topic_shift_at or args.no_topic_shift or args.batch > 1 or args.lookahead or args.l2_resident_mb:
+        return None
+    return (f"group ranks of every layer redrawn (new W2) for tokens {distinct // 2}..{distinct - 1} of each "
+            f"{distinct}-token cycle, and back at the cycle's start")
+
+
 def bench_config(spec, batch: int, n_layers: int, distinct: int, normalize: bool, zero_skip: bool, world: int,
-                 replicas_note: str | None) -> dict:
+                 replicas_note: str | None, topic: str | None = None) -> dict:
     """The workload part of the line's config: identical for both arms."""
     held, read = stack_bytes(spec, n_layers)
     if read > L2_BYTES:
@@ -299,6 +315,7 @@ def bench_config(spec, batch: int, n_layers: int, distinct: int, normalize: bool
         "normalize": ("each layer is fed x_l / rms(x_l), a harness stand-in for the rest of the block (torch ops "
                       "outside the library); residual x_{l+1} = x_l + y_l") if normalize else None,
         "zero_skip": zero_skip,
+        "topic_shift": topic,
         "l2": l2,
         "parallelism": "replicas" if world > 1 else "single",
     }
@@ -365,12 +382,21 @@ def run_ours(args, world, rank, local):
     nL = spec.layers
     want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
 
-    # ---- layers (generated on the device, packed, originals freed)
-    layers, host0 = [], None
+    P = max(1, min(args.tokens, spec.tokens))
+    topic = topic_shift_note(spec, args, P)
+    # ---- layers (generated on the device, packed, originals freed); with a
+    # topic shift, a second set whose W2 places the redrawn group ranks
+    layers, layers_t1, host0 = [], [], None
     with torch.cuda.stream(stream):
         for l in range(nL):
             w = W.make_layer(spec, seed=args.seed, layer=l, device=dev)
             layers.append(sffn.Layer.from_weights(w, spec.group_size, spec.act, max_batch=Bt, stream=stream))
+            if topic:
+                w1 = dict(w)
+                w1["W2"] = W.make_w2_topic(spec, args.seed, l, 1, w["W1"], w["perm"])
+                layers_t1.append(sffn.Layer.from_weights(w1, spec.group_size, spec.act, max_batch=Bt,
+                                                         stream=stream))
+                del w1
             if l == 0 and want_cpu:
                 host0 = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v)
                          for k, v in w.items()}
@@ -392,8 +418,9 @@ def run_ours(args, world, rank, local):
         for l in range(nL):
             layers[l].set_zero_skip(True, rows_read[l:l + 1])
     if prefetch_next:
-        for l in range(nL):
-            layers[l].set_next(layers[(l + 1) % nL])
+        for Ls in (layers, layers_t1):
+            for l in range(len(Ls)):
+                Ls[l].set_next(Ls[(l + 1) % nL])
     # one-layer-ahead prediction: the predictor and the FFN run on disjoint SMs
     lookahead = args.lookahead if Bt == 1 else 0
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -403,8 +430,22 @@ def run_ours(args, world, rank, local):
         for L in layers:
             L.set_grid(n_sms - lookahead, lookahead)
 
+    # ---- whole-stack kernel: one launch per token (per topic, one stack)
+    use_stack = bool(args.stack)
+    if use_stack and (Bt != 1 or normalize or lookahead or zero_skip or args.l2_resident_mb):
+        raise SystemExit("--stack runs B = 1 without --normalize, --lookahead, --zero-skip or --l2-resident-mb")
+    if use_stack:
+        stacks = [sffn.Stack(layers)] + ([sffn.Stack(layers_t1)] if topic else [])
+        stacks = stacks + stacks[:1] if len(stacks) == 1 else stacks
+        smasks = [stacks[0].masks(device=dev) for _ in range(2)]
+        sws = stacks[0].workspace(device=dev)
+        sxs = torch.empty(nL, spec.d, device=dev)
+
     # ---- buffers
-    P = max(1, min(args.tokens, spec.tokens))
+    sets = (layers, layers_t1 if topic else layers)
+
+    def topic_of(t):
+        return 1 if topic and (t % P) >= P // 2 else 0
     X = W.spec_tokens(spec, P, seed=args.seed, batch=Bt, device=dev).contiguous()  # [P,B,d]
     gw = (spec.n_groups + 31) // 32
     # group masks of all layers, double-buffered by token parity: the momentum
@@ -443,6 +484,8 @@ def run_ours(args, world, rank, local):
     # product + finisher, scores product + finisher, mask views, up/gate
     # product + activation, down product + finisher.
     launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0) + (1 if l2_groups else 0)
+    if use_stack:
+        launches_per_step = 1 + 1 + (1 if spec.anb else 0)
     if lookahead:
         launches_per_step += nL   # sffn_predict adds the mask-views kernel
         pstream = torch.cuda.Stream(device=dev)
@@ -450,19 +493,20 @@ def run_ours(args, world, rank, local):
         ev_x = [torch.cuda.Event() for _ in range(nL)]
         ev_p = [torch.cuda.Event() for _ in range(nL)]
 
-    def layers_pass(x, saved=None):
+    def layers_pass(x, saved=None, tp=0):
         """One token through every layer on `stream`; returns the last x_out.
         Exact method: sffn_decode_step per layer. Look-ahead: layer 0 is
         predicted from its own input, layer l + 1 from x_l on `pstream` while
         layer l's FFN runs (sffn_forward). `saved` collects each layer's input."""
         outb = (xa, xb)
+        Ls = sets[tp]
         if normalize:
             resid = x
             for l in range(nL):
                 xn = rms_normalize(resid)
                 if saved is not None:
                     saved.append(xn.clone())
-                sffn.sffn_decode_step(layers[l].handle, xn, Bt, spec.thres, masks[l], ybuf, None, ws, stream)
+                sffn.sffn_decode_step(Ls[l].handle, xn, Bt, spec.thres, masks[l], ybuf, None, ws, stream)
                 resid = resid + ybuf
             return resid
         if lookahead:
@@ -472,7 +516,7 @@ def run_ours(args, world, rank, local):
             if saved is not None:
                 saved.append(x.clone())
             if not lookahead:
-                sffn.sffn_decode_step(layers[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
+                sffn.sffn_decode_step(Ls[l].handle, x, Bt, spec.thres, masks[l], ybuf, xo, ws, stream)
             else:
                 if l + 1 < nL:
                     ev_x[l].record(stream)
@@ -485,10 +529,24 @@ def run_ours(args, world, rank, local):
             x = xo
         return x
 
+    def stack_step(t, xin=None):
+        """Token t through the whole stack in one launch, then its momentum
+        step (and lambda step) on the same stream: the stack kernel holds
+        every SM, so a concurrent branch would only delay it."""
+        par = t % 2
+        x = (X[t % P] if xin is None else xin)[0]
+        sffn.sffn_stack_decode(stacks[topic_of(t)].handle, x, sxs, None, spec.thres, smasks[par], sws, stream)
+        sffn.tam_update(tam.handle, 0, nL, smasks[par].gmask, gw, -1.0, spec.tam_eps, K, outs, stream)
+        if spec.anb:
+            sffn.tam_adapt(tam.handle, 0, nL, stalls[t % P], spec.anb_alpha, spec.anb_lo, spec.anb_hi, stream)
+        return sxs[nL - 1:nL]
+
     def step(t, xin=None, saved=None):
         """Token t through every layer; in parallel, on a side stream, the
         momentum update (and lambda step) of token t-1, whose group masks sit in
         the other parity buffer. One momentum update per step."""
+        if use_stack:
+            return stack_step(t, xin)
         par = t % 2
         ev_fork.record(stream)
         side.wait_event(ev_fork)
@@ -501,7 +559,7 @@ def run_ours(args, world, rank, local):
         x = X[t % P] if xin is None else xin
         for l in range(nL):
             set_tam_mask(l, gmask_buf[par, l].data_ptr())
-        x = layers_pass(x, saved)
+        x = layers_pass(x, saved, topic_of(t))
         stream.wait_event(ev_join)
         return x
 
@@ -529,7 +587,10 @@ def run_ours(args, world, rank, local):
                 raise SystemExit(f"{spec.name}: the residual stream overflowed within {nL} layers (a gated FFN grows "
                                  "with the square of its input and this stack has no block normalisation); "
                                  "use --layers to shorten it")
-            if Bt == 1:
+            if use_stack:
+                counts[t] = smasks[t % 2].count.cpu().numpy()
+                tok_counts[t] = counts[t]
+            elif Bt == 1:
                 counts[t] = torch.stack([m.count[0] for m in masks]).cpu().numpy()
                 tok_counts[t] = counts[t]
                 if zero_skip:
@@ -537,7 +598,7 @@ def run_ours(args, world, rank, local):
             else:
                 counts[t] = torch.stack([m.ucount[0] for m in masks]).cpu().numpy()
                 tok_counts[t] = torch.stack([m.count.sum() for m in masks]).cpu().numpy()
-    for L in layers:
+    for L in layers + layers_t1:
         L.check_error(stream)
 
     def cost(t_, l_):
@@ -594,8 +655,11 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop() if sampler else None
     step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     elapsed_ms, value = replica_job_rate(evs[0].elapsed_time(evs[-1]), Bt * args.steps, world, dev)
-    for L in layers:
+    for L in layers + layers_t1:
         L.check_error(stream)
+    if use_stack:
+        for st_ in stacks:
+            st_.check_error(stream)
     sffn.tam_check_error(tam.handle, stream)
     toks = [(t_start + i) % P for i in range(args.steps)]
     timed_bytes = float(sum(metric_bytes[t] for t in toks))
@@ -606,11 +670,21 @@ def run_ours(args, world, rank, local):
     # ---- traced pass: per-kernel durations (events around each kernel)
     R = min(args.profile_steps, P)
     KN = KERNELS if Bt == 1 else KERNELS_BATCH
+    if use_stack:
+        KN = ("decode_stack",)
     ev = {k: [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
               for _ in range(R)] for k in KN}
     tam_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
     with torch.cuda.stream(stream):
         for r in range(R):
+            if use_stack:
+                ev["decode_stack"][r][0][0].record(stream)
+                sffn.sffn_stack_decode(stacks[0].handle, X[r % P][0], sxs, None, spec.thres, smasks[0], sws, stream)
+                ev["decode_stack"][r][0][1].record(stream)
+                tam_ev[r][0].record(stream)
+                sffn.tam_update(tam.handle, 0, nL, smasks[0].gmask, gw, -1.0, spec.tam_eps, K, outs, stream)
+                tam_ev[r][1].record(stream)
+                continue
             for l in range(nL):
                 sffn.sffn_layer_set_trace(layers[l].handle, [ev[k][r][l][0] for k in KN],
                                           [ev[k][r][l][1] for k in KN])
@@ -624,6 +698,13 @@ def run_ours(args, world, rank, local):
         sffn.sffn_layer_set_trace(L.handle)
     per_kernel = {}
     for k in KN:
+        if k == "decode_stack":
+            # one launch per token: its algorithmic bytes are the whole token's
+            durs = [ev[k][r][0][0].elapsed_time(ev[k][r][0][1]) for r in range(R)]
+            kb = [sum(cost(r % P, l)["metric"] for l in range(nL)) for r in range(R)]
+            per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
+                             "gbs": sum(kb) / (sum(durs) / 1e3) / 1e9}
+            continue
         durs = [ev[k][r][l][0].elapsed_time(ev[k][r][l][1]) for r in range(R) for l in range(nL)]
         kb = [cost(r % P, l)["kernels"][k] for r in range(R) for l in range(nL)]
         per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
@@ -739,11 +820,18 @@ def run_ours(args, world, rank, local):
     # ---- harness cost (the --normalize stand-in alone, same count per step)
     harness_us = 0.0
     if normalize:
+        # captured like the step (one graph of a token's worth of harness ops)
+        hg = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             hx = X[0].clone()
+            with torch.cuda.graph(hg, stream=stream):
+                hy = hx
+                for i in range(nL):
+                    hy = rms_normalize(hy) + ybuf
+            hg.replay()
             e0.record(stream)
-            for i in range(nd * nL):
-                hx = rms_normalize(hx) + ybuf
+            for i in range(nd):
+                hg.replay()
             e1.record(stream)
         torch.cuda.synchronize()
         harness_us = 1e3 * e0.elapsed_time(e1) / (nd * nL)
@@ -778,8 +866,11 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": bench_config(spec, Bt, nL, P, normalize, zero_skip, world, replicas_note),
-        "run": {"graphs": graphs is not None, "l2_prefetch_next": prefetch_next,
+        "config": bench_config(spec, Bt, nL, P, normalize, zero_skip, world, replicas_note, topic),
+        "run": {"kernels": "one whole-stack kernel per token (sffn_stack_decode)" if use_stack
+                           else "four kernels per layer (sffn_decode_step)" if Bt == 1
+                           else "batched tensor-core path (sffn_decode_step, B > 1)",
+                "graphs": graphs is not None, "l2_prefetch_next": prefetch_next and not use_stack,
                 "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
                 "timed_bytes_per_step_gb": round(timed_bytes / args.steps / 1e9, 4),
                 "l2_between_steps": "not flushed: every step reads more distinct weights than L2 holds"
@@ -916,10 +1007,13 @@ def cpu_worker(tmp: str) -> None:
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
 
-def host_layer(W, O, spec, seed, layer, dev):
-    """Stored host copies of one layer, in the form the oracle reads."""
+def host_layer(W, O, spec, seed, layer, dev, topic=0):
+    """Stored host copies of one layer, in the form the oracle reads (topic 1:
+    the W2 of the redrawn group ranks)."""
     import torch
     w = W.make_layer(spec, seed=seed, layer=layer, device=dev)
+    if topic:
+        w["W2"] = W.make_w2_topic(spec, seed, layer, topic, w["W1"], w["perm"])
     host = {k: (W.stored_numpy(v) if torch.is_tensor(v) and v.dtype != torch.int32 else v) for k, v in w.items()}
     host["perm"] = w["perm"].cpu().numpy()
     host["b2f"] = None if w["b2"] is None else w["b2"].double().cpu().numpy()
@@ -960,18 +1054,21 @@ def run_reference(args, world, rank, local):
     nL = spec.layers
     P = max(1, min(args.tokens, spec.tokens))
     dev = "cuda" if torch.cuda.is_available() else "cpu"
+    topic = topic_shift_note(spec, args, P)
     hosts = [host_layer(W, O, spec, args.seed, l, dev) for l in range(nL)]
+    hosts1 = [host_layer(W, O, spec, args.seed, l, dev, topic=1) for l in range(nL)] if topic else hosts
     X = W.spec_tokens(spec, P, seed=args.seed, batch=Bt).double().numpy()     # [P, B, d]
 
     def rms(v):
         return v / np.sqrt(np.mean(v * v))
 
     def one(t):
+        hs = hosts1 if topic and (t % P) >= P // 2 else hosts
         for b in range(Bt):
             x = X[t % P, b]
             for l in range(nL):
                 xin = rms(x) if args.normalize else x
-                x = x + oracle_layer(O, spec, hosts[l], xin)
+                x = x + oracle_layer(O, spec, hs[l], xin)
 
     t_begin = time.perf_counter()
     warm = []
@@ -1002,7 +1099,8 @@ def run_reference(args, world, rank, local):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
         "steps": K_run, "warmup": args.warmup, "ms_per_step": round(1e3 * sec / K_run, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": bench_config(spec, Bt, nL, P, bool(args.normalize), bool(args.zero_skip), world, replicas_note),
+        "config": bench_config(spec, Bt, nL, P, bool(args.normalize), bool(args.zero_skip), world, replicas_note,
+                               topic),
         "ms_per_step_pct": percentiles_ms([1e3 * v for v in per]),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},

@@ -328,6 +328,63 @@ sffn_status sffn_decode_step(const sffn_layer* layer, const float* x, int32_t B,
 sffn_status sffn_decode_step_static_ws(const sffn_layer* layer, const float* x, int32_t B, float thres,
                                        const sffn_masks* masks, float* y, float* x_out, sffn_stream stream);
 
+/* ---------------------------------------------------------------- whole stack */
+
+/* A stack of layers decoded one token at a time by ONE kernel launch: for
+ * every layer in order, the predictor (PowerInfer §5.1), the threshold, the
+ * sparse FFN over the predicted rows (§5.3-§5.4) and the residual
+ * x_{l+1} = x_l + y_l -- the computation of sffn_decode_step at B = 1 with
+ * x_out chaining the layers, with the same summation orders (hid, masks,
+ * index lists, y and x_{l+1} are bit-identical to that chain on the same
+ * inputs). One thread block per SM runs the whole token; grid-wide barriers
+ * separate the phases, and each block streams the next phases' predictor
+ * weights while the barriers and the other phases run. The layers must
+ * share d, f, h, group_size, act and storage, use 16-bit weights in
+ * SFFN_FFN_ROWS form, and keep at most 32 KB per neuron of up/gate rows
+ * (d <= 8192 for ReGLU/SwiGLU, d <= 16384 for ReLU); other shapes return
+ * UNSUPPORTED (use the per-layer calls). The stack keeps the layers' packed
+ * arrays' addresses, not the layers: they must outlive it (re-packing a layer
+ * in place is fine). Per-layer options (sffn_layer_set_next, _set_grid,
+ * _set_l2_resident, _set_zero_skip) do not apply to the stack kernel.
+ * Errors: INVALID_ARG (NULL, n_layers outside [1, 4096], layers that differ
+ * or live on other devices), UNSUPPORTED, OOM, CUDA. */
+typedef struct sffn_stack sffn_stack;
+sffn_status sffn_stack_create(const sffn_layer* const* layers /* host array [n_layers] */, int32_t n_layers,
+                              sffn_stack** out);
+
+/* Bytes of caller workspace sffn_stack_decode needs (0 if stack is NULL):
+ * the hidden vector and one partial sum of y per SM. */
+size_t sffn_stack_workspace_bytes(const sffn_stack* stack);
+
+/* One decode token through every layer (device pointers, fp32):
+ *   x0  [d]            input of layer 0 (16-byte aligned); it may be one of
+ *                      xs's rows, e.g. the previous token's output
+ *                      xs + (n_layers-1)*d, and is otherwise not written;
+ *   xs  [n_layers][d]  written: xs[l] = x_l + y_l, the input of layer l+1
+ *                      (x_0 = x0); xs[n_layers-1] is the token's output;
+ *   ys  [n_layers][d]  written if not NULL: y_l;
+ *   masks: each field is a per-layer array, rows [n_layers][...] as for one
+ *     token: nmask [n_layers][f/32] (required), gmask [n_layers][gw],
+ *     idx [n_layers][f], count [n_layers] (each optional, NULL = not
+ *     written); the union fields are ignored.
+ *   ws: at least sffn_stack_workspace_bytes(stack), 256-byte aligned.
+ * The kernel's grid barrier state lives in the stack handle, so calls on one
+ * stack must not overlap on the GPU (order them on one stream); different
+ * stacks may run concurrently only if the GPU can hold both grids, which one
+ * GB300 cannot (each holds every SM). The launch needs every SM: work that
+ * occupies SMs at the same time only delays it. Allocates nothing, does not
+ * synchronize, may be captured in a CUDA graph. A bounded wait that runs out
+ * is reported by sffn_stack_check_error.
+ * Errors: INVALID_ARG, CUDA. */
+sffn_status sffn_stack_decode(const sffn_stack* stack, const float* x0, float* xs, float* ys, float thres,
+                              const sffn_masks* masks, void* ws, size_t ws_bytes, sffn_stream stream);
+
+/* Synchronize the stream, read and clear the stack's device error word (OK,
+ * TIMEOUT or DEVICE); after an error it also resets the grid barrier so the
+ * next call starts clean. */
+sffn_status sffn_stack_check_error(const sffn_stack* stack, sffn_stream stream);
+void sffn_stack_destroy(sffn_stack* stack);
+
 /* ---------------------------------------------------------------- TAM */
 
 /* Momentum state for n_layers layers of n_groups groups (1..1024): scores
