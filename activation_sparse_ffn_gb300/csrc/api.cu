@@ -652,10 +652,10 @@ sffn_status sffn_stack_create(const sffn_layer* const* layers, int32_t n_layers,
     stack_fill_layer_desc(*layers[l], table + one * l);
   }
   cudaError_t e = cudaMalloc(&S->dev_layers, one * n_layers);
-  if (e == cudaSuccess) e = cudaMalloc((void**)&S->bar, 256);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&S->bar, kStackBarBytes);
   if (e == cudaSuccess) e = cudaMalloc((void**)&S->err, 256);
   if (e == cudaSuccess) e = cudaMemcpy(S->dev_layers, table, one * n_layers, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = cudaMemset(S->bar, 0, 256);
+  if (e == cudaSuccess) e = cudaMemset(S->bar, 0, kStackBarBytes);
   if (e == cudaSuccess) e = cudaMemset(S->err, 0, 256);
   if (e == cudaSuccess) e = configure_stack_kernels(*L0);
   delete[] table;
@@ -706,7 +706,7 @@ sffn_status sffn_stack_check_error(const sffn_stack* S, sffn_stream stream) {
   sffn_status rc = read_error_word(S->err, (cudaStream_t)stream);
   if (rc == SFFN_ERR_TIMEOUT || rc == SFFN_ERR_DEVICE) {
     // a kernel that wound down may have left the grid barrier half-way
-    cudaError_t e = cudaMemset(S->bar, 0, 256);
+    cudaError_t e = cudaMemset(S->bar, 0, kStackBarBytes);
     if (e != cudaSuccess) return cuda_fail(e, "sffn_stack_check_error: reset the grid barrier");
   }
   return rc;

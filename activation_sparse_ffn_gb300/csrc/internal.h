@@ -71,7 +71,7 @@ struct sffn_stack {
   int device = 0;
   const sffn_layer** layers = nullptr;  // host array [n_layers]
   void* dev_layers = nullptr;           // device table of the layers' packed arrays
-  unsigned* bar = nullptr;              // grid barrier: arrivals, generation
+  unsigned* bar = nullptr;              // grid barrier: arrival counter, generation
   uint32_t* err = nullptr;              // device error word
 };
 
@@ -128,6 +128,7 @@ cudaError_t launch_tam_adapt(tam_state& S, int layer0, int n_layers, const uint8
 cudaError_t launch_selftest_timeout(uint32_t* err, int limit_us, cudaStream_t st);
 
 // Whole-stack decode kernel (stack.cu).
+constexpr size_t kStackBarBytes = 256;   // grid barrier words
 bool stack_supported(const sffn_layer& L, std::string* why);
 cudaError_t configure_stack_kernels(const sffn_layer& L);
 size_t stack_ws_bytes(const sffn_layer& L);

@@ -41,6 +41,8 @@ constexpr int kSC = kSW * 32;           // consumer threads
 constexpr int kSThreads = kSC + 32;     // + the producer warp
 constexpr uint32_t kSB = 32768;         // ring stage bytes
 constexpr int kReduceGroupsS = 32;      // partial groups of the y reduction (as k_ffn_reduce)
+constexpr int kReducePer = 8;           // partials per group (blocks <= 256), zeros past the last
+constexpr int kWordsPerThread = 8;      // mask words per consumer thread in the scan (f <= 65536)
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kSC) : "memory"); }
 
@@ -130,14 +132,15 @@ struct StackParams {
   uint32_t* err;
 };
 
-// Grid-wide barrier among the consumer warps of every block. `ok` is this
-// thread's state; if any consumer thread of the block has failed, the block
-// does not arrive. Returns, uniformly over the block's consumers, false if
-// the block failed, a wait ran out or another block failed (the reason is in
-// the error word).
+// Grid-wide barrier among the consumer warps of every block: an arrival
+// counter and a generation word in global memory. The last block to arrive
+// resets the counter and advances the generation (release); the others poll
+// the generation (acquire). `ok_in` is this thread's state: if any consumer
+// thread of the block has failed, the block does not arrive. Returns,
+// uniformly over the block's consumers, false if the block failed, a wait ran
+// out or another block failed (the reason is in the error word).
 __device__ bool grid_sync(const StackParams& p, bool ok_in, unsigned* s_gen, int* s_ok) {
-  // every consumer thread of this block has issued its global writes
-  if (cbar_or(!ok_in)) return false;
+  if (cbar_or(!ok_in)) return false;  // every consumer thread has issued its global writes
   if (threadIdx.x == 0) {
     int ok = ld_volatile_u32(p.err) == 0;
     const unsigned gen = *s_gen;
@@ -434,14 +437,24 @@ __global__ void __launch_bounds__(kSThreads, 1) k_decode_stack(const StackParams
       const uint32_t* nm = p.nmask + (size_t)l * p.nw;
       int total, lo, n_local;
       {
+        // all words requested at once (coalesced, independent loads), then
+        // each thread counts a contiguous range of them
+        uint32_t wv[kWordsPerThread];
+#pragma unroll
+        for (int i = 0; i < kWordsPerThread; ++i) {
+          const int w = threadIdx.x + i * kSC;
+          wv[i] = w < p.nw ? __ldcg(nm + w) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kWordsPerThread; ++i) {
+          const int w = threadIdx.x + i * kSC;
+          if (w < p.nw) s_words[w] = wv[i];
+        }
+        cbar();
         const int per = (p.nw + kSC - 1) / kSC;
         const int a0 = min(p.nw, (int)threadIdx.x * per), a1 = min(p.nw, a0 + per);
         int cnt = 0;
-        for (int w = a0; w < a1; ++w) {
-          const uint32_t m = __ldcg(nm + w);
-          s_words[w] = m;
-          cnt += __popc(m);
-        }
+        for (int w = a0; w < a1; ++w) cnt += __popc(s_words[w]);
         int off = cons_exclusive_scan(cnt, s_tmp, &total);
         for (int w = a0; w < a1; ++w) {
           s_off[w] = off;
@@ -579,40 +592,49 @@ __global__ void __launch_bounds__(kSThreads, 1) k_decode_stack(const StackParams
       if (!(ok = grid_sync(p, ok, &s_gen, &s_ok))) break;
       // ---------------------------------------------------------- R
       {
-        // float4 columns [c0, c1) of this block; one warp per column, lane g
-        // adds partials g, g + 32, ... and the 32 group sums are added in
+        // float4 columns [c0, c1) of this block; for each column lane g of a
+        // warp adds partials g, g + 32, ... and the 32 group sums are added in
         // group order (the order of k_ffn_reduce)
         const int cols = d / 4;
         const int c0 = (int)((long long)cols * b / nb), c1 = (int)((long long)cols * (b + 1) / nb);
-        const int per = (nb + kReduceGroupsS - 1) / kReduceGroupsS;
-        const int perpad = per <= 4 ? 4 : per <= 8 ? 8 : 16;
         float* yl = p.ys ? p.ys + (size_t)l * d : nullptr;
         float* xo = p.xs + (size_t)l * d;
-        for (int c = c0 + warp; c < c1; c += kSW) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int i = 0; i < perpad; ++i) {
-            const int pi = lane + i * kReduceGroupsS;
-            const float4 v = pi < nb ? ld_dep4(p.partials + (size_t)pi * d + (size_t)c * 4)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i == 0) {
-              acc = v;
-            } else {
-              acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        // two columns per warp and pass, every partial load issued before any add
+        for (int cb = c0 + warp; cb < c1; cb += 2 * kSW) {
+          float4 v[2][kReducePer];
+          float xv[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c = cb + k * kSW;
+            xv[k] = (lane < 4 && c < c1) ? ld_dep(x + (size_t)c * 4 + lane) : 0.f;
+#pragma unroll
+            for (int i = 0; i < kReducePer; ++i) {
+              const int pi = lane + i * kReduceGroupsS;
+              v[k][i] = (c < c1 && pi < nb) ? ld_dep4(p.partials + (size_t)pi * d + (size_t)c * 4)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
-          s_red[warp][lane][0] = acc.x;
-          s_red[warp][lane][1] = acc.y;
-          s_red[warp][lane][2] = acc.z;
-          s_red[warp][lane][3] = acc.w;
-          __syncwarp();
-          if (lane < 4) {
-            float s = s_red[warp][0][lane];
-            for (int g = 1; g < kReduceGroupsS; ++g) s += s_red[warp][g][lane];
-            const float xv = ld_dep(x + (size_t)c * 4 + lane);
-            if (yl) yl[(size_t)c * 4 + lane] = s;
-            __stcg(xo + (size_t)c * 4 + lane, xv + s);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c = cb + k * kSW;
+            float4 acc = v[k][0];
+#pragma unroll
+            for (int i = 1; i < kReducePer; ++i) {
+              acc.x += v[k][i].x; acc.y += v[k][i].y; acc.z += v[k][i].z; acc.w += v[k][i].w;
+            }
+            s_red[warp][lane][0] = acc.x;
+            s_red[warp][lane][1] = acc.y;
+            s_red[warp][lane][2] = acc.z;
+            s_red[warp][lane][3] = acc.w;
+            __syncwarp();
+            if (lane < 4 && c < c1) {
+              float sum = s_red[warp][0][lane];
+              for (int g = 1; g < kReduceGroupsS; ++g) sum += s_red[warp][g][lane];
+              if (yl) yl[(size_t)c * 4 + lane] = sum;
+              __stcg(xo + (size_t)c * 4 + lane, xv[k] + sum);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       if (l + 1 < p.n_layers && !(ok = grid_sync(p, ok, &s_gen, &s_ok))) break;
@@ -659,6 +681,10 @@ bool stack_supported(const sffn_layer& L, std::string* why) {
   const size_t rowB = (size_t)D.d * 2;
   if (rowB * (act_gated(D.act) ? 2 : 1) > kSB) {
     *why = "one neuron's up/gate rows must fit a 32 KB ring stage (d <= 8192 gated, d <= 16384 otherwise)";
+    return false;
+  }
+  if (L.num_sms > kReduceGroupsS * kReducePer) {
+    *why = "the stack kernel's reduction handles at most 256 SMs";
     return false;
   }
   StackShape s = stack_shape(L, L.num_sms, L.smem_optin);

@@ -117,10 +117,10 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# DRAM counters of one kernel, taken by ncu on a named capture and stored
-# beside its summary in profiles/; valid only while the kernel's sources hash
-# to the value recorded with them.
-TRAFFIC_FILES = {"ffn": "profiles/k_ffn_dram_traffic.json"}
+# DRAM counters of one kernel on one workload, taken by ncu on a named
+# capture and stored beside its summary in profiles/ (one file per workload);
+# valid only while the kernel's sources hash to the value recorded with them.
+TRAFFIC_FILES = {"ffn": "profiles/k_ffn_dram_traffic_{workload}.json"}
 
 
 def sources_sha256(paths) -> str:
@@ -140,7 +140,10 @@ def measured_traffic(kernel: str, units_per_launch: float, prefetch: bool, workl
     depend on the row length and storage, so a capture only serves the
     workload it was taken on."""
     rel = TRAFFIC_FILES.get(kernel)
-    if rel is None or not os.path.exists(os.path.join(ROOT, rel)):
+    if rel is None:
+        return None
+    rel = rel.format(workload=workload)
+    if not os.path.exists(os.path.join(ROOT, rel)):
         return None
     with open(os.path.join(ROOT, rel)) as fh:
         d = json.load(fh)

@@ -83,19 +83,22 @@ def _write_capture(tmp_path):
         "sources": [str(src)],
     }
     d["sources_sha256"] = bench.sources_sha256(d["sources"])      # absolute paths join to themselves
-    cap = tmp_path / "cap.json"
+    cap = tmp_path / "cap_some_layer.json"
     cap.write_text(json.dumps(d))
     return src, cap
 
 
 def test_traffic_scales_by_active_rows_only_for_its_workload_and_sources(tmp_path, monkeypatch):
     src, cap = _write_capture(tmp_path)
-    monkeypatch.setitem(bench.TRAFFIC_FILES, "ffn", str(cap))
+    monkeypatch.setitem(bench.TRAFFIC_FILES, "ffn", str(tmp_path / "cap_{workload}.json"))
     # 49 KB per neuron once the 16 MB prefetch is taken out; the prefetch is added back when on
     assert bench.measured_traffic("ffn", 2000, False, "some_layer") == pytest.approx(2000 * 49_000)
     assert bench.measured_traffic("ffn", 2000, True, "some_layer") == pytest.approx(2000 * 49_000 + 16_000_000)
-    # bytes per neuron of one layer shape say nothing about another
+    # bytes per neuron of one layer shape say nothing about another (no capture of it)
     assert bench.measured_traffic("ffn", 2000, True, "another_layer") is None
+    cap.rename(tmp_path / "cap_another_layer.json")      # a capture filed under the wrong workload
+    assert bench.measured_traffic("ffn", 2000, True, "another_layer") is None
+    cap = (tmp_path / "cap_another_layer.json").rename(tmp_path / "cap_some_layer.json")
     src.write_text("kernel source v2\n")
     assert bench.measured_traffic("ffn", 2000, True, "some_layer") is None
     assert bench.measured_traffic("no_such_kernel", 2000, True, "some_layer") is None
