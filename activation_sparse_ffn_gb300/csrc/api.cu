@@ -33,8 +33,28 @@ sffn_status check_device(int want) {
   return SFFN_OK;
 }
 
+// Largest batch the automatic choice gives to the CUDA-core arm: on GB300 it
+// beats the tensor-core products at B = 2 and loses from B = 3 on (Falcon-40B-
+// shaped layer: 63.4 against 67.2 us at B = 2, 79.7 against 70.9 at B = 3).
+constexpr int kAutoCudaCoreMaxBatch = 2;
+
+// Whether a batched call on this layer runs the CUDA-core arm (batch_cc.cu)
+// rather than the tensor-core products (batch.cu).
+bool use_cuda_cores(const sffn_layer& L, int B) {
+  if (L.batch_path == SFFN_BATCH_CUDA_CORES) return B <= kCcMaxBatch;
+  if (L.batch_path == SFFN_BATCH_AUTO && B <= kAutoCudaCoreMaxBatch) {
+    std::string why;
+    return batch_cc_supported(L, B, &why);
+  }
+  return false;
+}
+
 size_t ws_bytes_for(const sffn_layer& L, int B) {
-  return B == 1 ? ws_layout(L, 1).total : batch_ws_layout(L, B).total;
+  if (B == 1) return ws_layout(L, 1).total;
+  // either arm may serve the call (sffn_layer_set_batch_path can change between calls)
+  const size_t tc = batch_ws_layout(L, B).total;
+  const size_t cc = B <= kCcMaxBatch ? batch_cc_ws_layout(L, B).total : 0;
+  return std::max(tc, cc);
 }
 
 sffn_status check_ws(const sffn_layer* L, int B, const void* ws, size_t ws_bytes) {
@@ -47,11 +67,17 @@ sffn_status check_ws(const sffn_layer* L, int B, const void* ws, size_t ws_bytes
 sffn_status check_batch(const sffn_layer* L, int B) {
   if (B < 1 || B > L->desc.max_batch) return invalid("B must be in [1, max_batch]");
   std::string why;
-  if (B > 1 && !batch_supported(*L, &why)) {
+  if (B > 1 && !(use_cuda_cores(*L, B) ? batch_cc_supported(*L, B, &why) : batch_supported(*L, &why))) {
     set_error(why);
     return SFFN_ERR_UNSUPPORTED;
   }
   return SFFN_OK;
+}
+
+cudaError_t launch_batched(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m,
+                           bool predict, bool forward, float* y, float* x_out, void* ws, cudaStream_t st) {
+  if (use_cuda_cores(L, B)) return launch_batch_cc(L, x, B, thres, m, predict, forward, y, x_out, ws, st);
+  return launch_batch(L, x, B, thres, m, predict, forward, y, x_out, ws, st);
 }
 
 // Records the layer's trace event for kernel slot k (if any) around `launch`.
@@ -194,6 +220,7 @@ sffn_status sffn_layer_create(const sffn_layer_desc* desc, sffn_layer** out) {
   if (e == cudaSuccess) e = configure_kernels(*L);
   if (e == cudaSuccess) e = configure_predict_kernels(*L);
   if (e == cudaSuccess) e = configure_batch_kernels(*L);
+  if (e == cudaSuccess) e = configure_batch_cc_kernels(*L);
   if (e != cudaSuccess) {
     rc = cuda_fail(e, "sffn_layer_create: kernel set-up");
     sffn_layer_destroy(L);
@@ -305,6 +332,21 @@ sffn_status sffn_layer_set_grid(sffn_layer* L, int32_t ffn_blocks, int32_t score
   return SFFN_OK;
 }
 
+sffn_status sffn_layer_set_batch_path(sffn_layer* L, int32_t path) {
+  if (!L) return invalid("layer is NULL");
+  if (path != SFFN_BATCH_AUTO && path != SFFN_BATCH_TENSOR && path != SFFN_BATCH_CUDA_CORES)
+    return invalid("path is not an sffn_batch_path");
+  L->batch_path = path;
+  return SFFN_OK;
+}
+
+int32_t sffn_layer_batch_arm(const sffn_layer* L, int32_t B) {
+  if (!L || B < 2 || B > L->desc.max_batch) return -1;
+  std::string why;
+  if (use_cuda_cores(*L, B)) return batch_cc_supported(*L, B, &why) ? SFFN_BATCH_CUDA_CORES : -1;
+  return batch_supported(*L, &why) ? SFFN_BATCH_TENSOR : -1;
+}
+
 sffn_status sffn_layer_set_zero_skip(sffn_layer* L, int32_t enable, int32_t* rows_read) {
   if (!L) return invalid("layer is NULL");
   if (rows_read && !aligned(rows_read, 4)) return invalid("rows_read must be 4-byte aligned");
@@ -383,7 +425,7 @@ sffn_status sffn_predict(const sffn_layer* L, const float* x, int32_t B, float t
   if (rc != SFFN_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   if (B > 1) {
-    cudaError_t e = launch_batch(*L, x, B, thres, m, true, false, nullptr, nullptr, ws, st);
+    cudaError_t e = launch_batched(*L, x, B, thres, m, true, false, nullptr, nullptr, ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "sffn_predict: launch");
     return SFFN_OK;
   }
@@ -406,7 +448,7 @@ sffn_status sffn_forward(const sffn_layer* L, const float* x, int32_t B, const s
   if (x_out && (x_out == y || !aligned(x_out, 16))) return invalid("x_out must be 16-byte aligned and differ from y");
   cudaStream_t st = (cudaStream_t)stream;
   if (B > 1) {
-    cudaError_t e = launch_batch(*L, x, B, 0.f, m, false, true, y, x_out, ws, st);
+    cudaError_t e = launch_batched(*L, x, B, 0.f, m, false, true, y, x_out, ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "sffn_forward: launch");
     return SFFN_OK;
   }
@@ -435,7 +477,7 @@ static sffn_status check_step(const sffn_layer* L, const float* x, int B, const 
 static sffn_status decode_step_launch(const sffn_layer* L, const float* x, int32_t B, float thres,
                                       const sffn_masks* m, float* y, float* x_out, void* ws, cudaStream_t st) {
   if (B > 1) {
-    cudaError_t e = launch_batch(*L, x, B, thres, m, true, true, y, x_out, ws, st);
+    cudaError_t e = launch_batched(*L, x, B, thres, m, true, true, y, x_out, ws, st);
     if (e != cudaSuccess) return cuda_fail(e, "sffn_decode_step: launch");
     return SFFN_OK;
   }

@@ -53,6 +53,8 @@ struct GemmArgs {
   size_t dmat_stride;       // floats from the first matrix's partials to the second's
   int grid;                 // CTAs launched
   uint32_t* err;
+  const unsigned char* pf;  // L2 hint: bytes this product's CTAs prefetch once their copies are issued (or null)
+  size_t pf_bytes;
 };
 
 // Work decomposition shared by the GEMM and its finishers (stream-K): the
@@ -295,6 +297,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   producers_done:
+    // L2 hint: this CTA's share of the next layer's hidden-layer weights,
+    // requested once its own copies are issued (null without a hint)
+    if (tid == 0 && g.pf && !*(volatile int*)&s_abort) {
+      const size_t units = g.pf_bytes / 16;
+      const size_t lo = units * blockIdx.x / gridDim.x * 16, hi = units * (blockIdx.x + 1) / gridDim.x * 16;
+      for (size_t o = lo; o < hi; o += 65536) prefetch_l2_bulk(g.pf + o, (uint32_t)min(hi - o, (size_t)65536));
+    }
     if (GATHER) tc::cp_async_wait_all();
     // let this CTA's TMA loads that no MMA consumed land before exiting
     if (tid == 0 && *(volatile int*)&s_abort) {
@@ -860,6 +869,15 @@ cudaError_t traced_b(const sffn_layer& L, int k, cudaStream_t st, F&& launch) {
   return e;
 }
 
+cudaError_t launch_batch_views(const sffn_layer& L, const sffn_masks* m, int B, uint32_t* unmask, int32_t* uidx,
+                               int32_t* ucount, bool predict, bool union_ready, cudaStream_t st) {
+  const int nw = L.nwords;
+  return launch_ex(k_b_views, dim3(B + 1), dim3(kViewThreadsB), (size_t)nw * 8, st, true, 1,
+                   static_cast<const uint32_t*>(m->nmask), B, nw, L.desc.f, L.n_groups, L.desc.group_size, L.gwords,
+                   predict ? m->idx : nullptr, predict ? m->count : nullptr, predict ? m->gmask : nullptr, unmask, uidx,
+                   ucount, m->ugmask, union_ready);
+}
+
 cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
                          bool forward, float* y, float* x_out, void* ws, cudaStream_t st) {
   const BatchWs w = batch_ws_layout(L, B);
@@ -985,6 +1003,10 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.D = reinterpret_cast<float*>(base + w.dy);
   dn.grid = grid;
   dn.err = L.err;
+  if (L.next) {  // sffn_layer_set_next: the next layer's W1 into L2 during the down product's tail
+    dn.pf = static_cast<const unsigned char*>(L.next->W1);
+    dn.pf_bytes = (size_t)L.next->desc.h * L.next->desc.d * L.next->wbytes;
+  }
   e = encode_rows(&dn.tmB, hhl, bf, fpad, 2 * npad, 2 * npad);
   if (e == cudaSuccess) e = traced_b(L, 3, st, [&] { return launch_down(L, npad, dn, st); });
   if (e != cudaSuccess) return e;

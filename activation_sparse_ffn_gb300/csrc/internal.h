@@ -48,6 +48,8 @@ struct sffn_layer {
   // and where to write how many were read (device, may be null)
   bool zero_skip = false;
   int32_t* rows_read = nullptr;
+  // batched calls (sffn_layer_set_batch_path): SFFN_BATCH_AUTO, _TENSOR or _CUDA_CORES
+  int batch_path = 0;
   // optional timing hooks (sffn_layer_set_trace)
   cudaEvent_t trace_begin[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaEvent_t trace_end[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -102,6 +104,21 @@ struct BatchWs {
 };
 BatchWs batch_ws_layout(const sffn_layer& L, int B);
 bool batch_supported(const sffn_layer& L, std::string* why);
+// Per-token views and the union views of a batch (k_b_views); union_ready:
+// the union words are already in unmask.
+cudaError_t launch_batch_views(const sffn_layer& L, const sffn_masks* m, int B, uint32_t* unmask, int32_t* uidx,
+                               int32_t* ucount, bool predict, bool union_ready, cudaStream_t st);
+
+// CUDA-core arm of the batched step for 2..kCcMaxBatch tokens (batch_cc.cu).
+constexpr int kCcMaxBatch = 4;
+struct BatchCcWs {
+  size_t hid = 0, unmask = 0, uidx = 0, ucount = 0, partials = 0, total = 0;
+};
+BatchCcWs batch_cc_ws_layout(const sffn_layer& L, int B);
+bool batch_cc_supported(const sffn_layer& L, int B, std::string* why);
+cudaError_t configure_batch_cc_kernels(const sffn_layer& L);
+cudaError_t launch_batch_cc(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
+                            bool forward, float* y, float* x_out, void* ws, cudaStream_t st);
 cudaError_t configure_batch_kernels(const sffn_layer& L);
 // Batched predictor (predict) and/or sparse FFN over the union (forward).
 cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres, const sffn_masks* m, bool predict,
@@ -152,6 +169,16 @@ size_t score_smem(const sffn_layer& L);
 int ffn_stages_for(const sffn_layer& L);
 size_t ffn_smem(const sffn_layer& L);
 int ffn_blocks(const sffn_layer& L);
+
+// Records the layer's trace event for kernel slot k (if any) around `launch`.
+template <typename F>
+cudaError_t traced_batch(const sffn_layer& L, int k, cudaStream_t st, F&& launch) {
+  cudaError_t e = cudaSuccess;
+  if (L.trace_begin[k]) e = cudaEventRecord(L.trace_begin[k], st);
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess && L.trace_end[k]) e = cudaEventRecord(L.trace_end[k], st);
+  return e;
+}
 
 // Launch helper: programmatic dependent launch and optional cluster size.
 template <typename... KArgs, typename... Args>

@@ -37,19 +37,34 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_tmp, int* tota
   return before + x - v;
 }
 
+// Most mask words a layer has: f <= 1024 groups of at most 64 slots.
+constexpr int kMaxMaskWords = 2048;
+
 // Loads nw mask words into s_words and writes each word's offset in the
 // ascending active list into s_off. Returns the number of active slots.
+// Every thread first requests all of its words at once (coalesced,
+// independent loads: one L2 round trip instead of one per word), then counts
+// a contiguous range of them from shared memory.
 template <int NT>
 __device__ __forceinline__ int scan_mask_words(const uint32_t* nmask, int nw, uint32_t* s_words,
                                                int* s_off, int* s_tmp) {
+  constexpr int kIter = (kMaxMaskWords + NT - 1) / NT;
+  uint32_t v[kIter];
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int w = (int)threadIdx.x + i * NT;
+    v[i] = w < nw ? ld_dep(nmask + w) : 0u;  // written by the previous kernel
+  }
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int w = (int)threadIdx.x + i * NT;
+    if (w < nw) s_words[w] = v[i];
+  }
+  __syncthreads();
   const int per = (nw + NT - 1) / NT;
   const int w0 = min(nw, (int)threadIdx.x * per), w1 = min(nw, w0 + per);
   int local = 0;
-  for (int w = w0; w < w1; ++w) {
-    const uint32_t m = ld_dep(nmask + w);  // written by the previous kernel
-    s_words[w] = m;
-    local += __popc(m);
-  }
+  for (int w = w0; w < w1; ++w) local += __popc(s_words[w]);
   int total;
   int off = block_exclusive_scan<NT>(local, s_tmp, &total);
   for (int w = w0; w < w1; ++w) {

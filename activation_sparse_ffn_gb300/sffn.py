@@ -96,6 +96,8 @@ _sig("sffn_layer_pack_q4", _c, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
 _sig("sffn_layer_set_grid", _c, _vp, _i32, _i32)
 _sig("sffn_layer_set_l2_resident", _c, _vp, _vp)
 _sig("sffn_layer_set_zero_skip", _c, _vp, _i32, _vp)
+_sig("sffn_layer_set_batch_path", _c, _vp, _i32)
+_sig("sffn_layer_batch_arm", _i32, _vp, _i32)
 _sig("sffn_layer_check_error", _c, _vp, _vp)
 _sig("sffn_layer_destroy", None, _vp)
 _sig("sffn_predict", _c, _vp, _vp, _i32, _f32, _P(MasksC), _vp, _size, _vp)
@@ -122,7 +124,7 @@ _sig("sffn_selftest_wait_timeout", _c, _vp, _i32, _vp)
 EXPORTS = [
     "sffn_status_string", "sffn_last_error", "sffn_version", "sffn_layer_validate", "sffn_layer_create",
     "sffn_layer_pack", "sffn_layer_get_desc", "sffn_layer_packed", "sffn_workspace_bytes", "sffn_layer_set_trace", "sffn_layer_set_next", "sffn_layer_set_grid",
-    "sffn_layer_set_l2_resident", "sffn_layer_set_zero_skip",
+    "sffn_layer_set_l2_resident", "sffn_layer_set_zero_skip", "sffn_layer_set_batch_path", "sffn_layer_batch_arm",
     "sffn_layer_pack_q8", "sffn_layer_pack_q4",
     "sffn_layer_check_error",
     "sffn_layer_destroy", "sffn_predict", "sffn_forward", "sffn_decode_step", "sffn_decode_step_static_ws", "sffn_decode_step_tam",
@@ -264,6 +266,21 @@ def sffn_layer_set_l2_resident(layer, resident=None) -> None:
 def sffn_layer_set_zero_skip(layer, enable: bool, rows_read=None) -> None:
     """Zero-skip of the B = 1 FFN (downT rows of neurons with h != 0 only); rows_read: device int32 or None."""
     _check(_lib.sffn_layer_set_zero_skip(layer, 1 if enable else 0, _ptr(rows_read)), "sffn_layer_set_zero_skip")
+
+
+BATCH_PATH = {"auto": 0, "tensor": 1, "cuda_cores": 2}
+
+
+def sffn_layer_set_batch_path(layer, path) -> None:
+    """Arithmetic of batched calls: "auto", "tensor" or "cuda_cores" (2 <= B <= 4)."""
+    _check(_lib.sffn_layer_set_batch_path(layer, BATCH_PATH[path] if isinstance(path, str) else path),
+           "sffn_layer_set_batch_path")
+
+
+def sffn_layer_batch_arm(layer, B: int) -> str | None:
+    """"tensor" or "cuda_cores": the arm serving a batch of B on this layer now (None: no arm)."""
+    a = int(_lib.sffn_layer_batch_arm(layer, B))
+    return {1: "tensor", 2: "cuda_cores"}.get(a)
 
 
 def sffn_workspace_bytes(layer, B: int) -> int:
@@ -534,6 +551,9 @@ class Layer:
         """sffn_layer_set_zero_skip; keeps a rows_read tensor alive while set."""
         sffn_layer_set_zero_skip(self.handle, enable, rows_read)
         self._rows_read = rows_read if enable else None
+
+    def set_batch_path(self, path) -> None:
+        sffn_layer_set_batch_path(self.handle, path)
 
     def set_next(self, other: "Layer | None") -> None:
         """L2 hint of sffn_layer_set_next; keeps ``other`` alive while set."""

@@ -36,6 +36,7 @@ METRIC = "sparse-FFN decode tokens/s at B=1; active-byte HBM GB/s as % of GB300 
 FALLBACK_HBM_GBS = 6800.0
 KERNELS = ("pred_hidden", "pred_scores", "ffn", "ffn_reduce")
 KERNELS_BATCH = ("hidden_gemm", "scores_gemm", "upgate_gemm", "down_gemm")
+KERNELS_BATCH_CC = ("cc_hidden", "cc_scores", "cc_ffn", "cc_reduce")
 BF16_PEAK_KEY = "bf16_tflops"
 
 
@@ -77,6 +78,8 @@ def parse_args():
     p.add_argument("--ref-budget-s", type=float, default=240.0,
                    help="reference arm: seconds its warm-up and timed steps may take; beyond it fewer steps are "
                         "timed and the line says so")
+    p.add_argument("--batch-path", choices=("auto", "tensor", "cuda_cores"), default="auto",
+                   help="B > 1: the tensor-core products, or the CUDA-core arm (2 <= B <= 4)")
     p.add_argument("--stack", action="store_true",
                    help="B = 1: run each token through the whole stack in one persistent kernel "
                         "(sffn_stack_decode) instead of four kernels per layer; the momentum step follows it")
@@ -249,7 +252,11 @@ def batch_layer_cost(spec, ucount: int, B: int, with_b2: bool) -> dict:
         "down_gemm": 2 * 2 * d * npad * (-(-ucount // 64) * 64),
     }
     metric = h * d * wb + f * h * wb + (f * 4 if with_b2 else 0) + ucount * spec.n_mats * d * wb + 2 * B * d * 4
-    return {"kernels": k, "flops": flops, "metric": metric}
+    # the CUDA-core arm (B <= 4): the same weight bytes, one kernel each for
+    # the hidden layer, the scores, the union FFN (all its rows) and the reduction
+    kcc = {"cc_hidden": h * d * wb + B * d * 4, "cc_scores": f * h * wb + (f * 4 if with_b2 else 0),
+           "cc_ffn": ucount * spec.n_mats * d * wb + B * d * 4, "cc_reduce": 3 * B * d * 4}
+    return {"kernels": k | kcc, "flops": flops, "metric": metric}
 
 
 def layer_bytes(spec, count: int, with_b2: bool, kept: int | None = None) -> dict:
@@ -409,9 +416,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     with_b2 = spec.bias_mode
+    cc_arm = False
+    if Bt > 1:
+        for L in layers + layers_t1:
+            L.set_batch_path(args.batch_path)
+        cc_arm = sffn.sffn_layer_batch_arm(layers[0].handle, Bt) == "cuda_cores"
     # L2 hint: each layer's FFN kernel warms the next layer's predictor weights
     # (the last layer warms layer 0 for the next token)
-    prefetch_next = Bt == 1 and not args.no_prefetch_next
+    prefetch_next = not args.no_prefetch_next
     # actual-activation zero-skip: each layer reports the downT rows it read
     zero_skip = bool(args.zero_skip)
     if zero_skip and Bt != 1:
@@ -486,7 +498,8 @@ def run_ours(args, world, rank, local):
     # B = 1: hidden, scores, fused FFN, reduction. B > 1: split of x, hidden
     # product + finisher, scores product + finisher, mask views, up/gate
     # product + activation, down product + finisher.
-    launches_per_step = nL * (4 if Bt == 1 else 10) + 1 + (1 if spec.anb else 0) + (1 if l2_groups else 0)
+    # CUDA-core arm (2 <= B <= 4): hidden, scores, views, union FFN, reduction.
+    launches_per_step = nL * (4 if Bt == 1 else 5 if cc_arm else 10) + 1 + (1 if spec.anb else 0) + (1 if l2_groups else 0)
     if use_stack:
         launches_per_step = 1 + 1 + (1 if spec.anb else 0)
     if lookahead:
@@ -672,7 +685,7 @@ def run_ours(args, world, rank, local):
 
     # ---- traced pass: per-kernel durations (events around each kernel)
     R = min(args.profile_steps, P)
-    KN = KERNELS if Bt == 1 else KERNELS_BATCH
+    KN = KERNELS if Bt == 1 else KERNELS_BATCH_CC if cc_arm else KERNELS_BATCH
     if use_stack:
         KN = ("decode_stack",)
     ev = {k: [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
@@ -712,7 +725,7 @@ def run_ours(args, world, rank, local):
         kb = [cost(r % P, l)["kernels"][k] for r in range(R) for l in range(nL)]
         per_kernel[k] = {"us": 1e3 * sum(durs) / len(durs), "bytes": sum(kb) / len(kb),
                          "gbs": sum(kb) / (sum(durs) / 1e3) / 1e9}
-        if Bt > 1:
+        if Bt > 1 and not cc_arm:
             kf = [cost(r % P, l)["flops"][k] for r in range(R) for l in range(nL)]
             per_kernel[k]["tflops"] = sum(kf) / (sum(durs) / 1e3) / 1e12
     tam_us = 1e3 * sum(a.elapsed_time(b) for a, b in tam_ev) / R
@@ -872,6 +885,7 @@ def run_ours(args, world, rank, local):
         "config": bench_config(spec, Bt, nL, P, normalize, zero_skip, world, replicas_note, topic),
         "run": {"kernels": "one whole-stack kernel per token (sffn_stack_decode)" if use_stack
                            else "four kernels per layer (sffn_decode_step)" if Bt == 1
+                           else "batched CUDA-core arm (sffn_decode_step, 2 <= B <= 4)" if cc_arm
                            else "batched tensor-core path (sffn_decode_step, B > 1)",
                 "graphs": graphs is not None, "l2_prefetch_next": prefetch_next and not use_stack,
                 "l2_resident": ({"mb": args.l2_resident_mb, "groups_per_layer": l2_groups} if l2_groups else None),
@@ -917,6 +931,7 @@ def run_ours(args, world, rank, local):
                              "note": "layers 1.. of every census token; layer 0 is predicted from its own input"}
     if Bt > 1:
         line["union_frac"] = round(float(counts.mean() / spec.f), 5)
+    if Bt > 1 and not cc_arm:
         tpk, _ = measured_tensor_peak()
         line["kernels_tflops"] = {k: round(v["tflops"], 2) for k, v in per_kernel.items()}
         line["tensor"] = {"kernel": dom, "achieved_tflops": round(pk["tflops"], 2), "peak": tpk,

@@ -218,10 +218,11 @@ typedef struct {
 
 sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* host, or NULL */);
 
-/* Optional L2 hint for a layer stack at B = 1. `next` names the layer whose
+/* Optional L2 hint for a layer stack. `next` names the layer whose
  * hot call follows this layer's on the same stream (in a stack: layer l + 1,
  * and for the last layer layer 0 of the next token), or NULL to turn the hint
- * off. Each block of this layer's sparse-FFN kernel then asks L2 to fetch its
+ * off. Each block of this layer's sparse-FFN kernel (B = 1), or of its down
+ * product on the tensor-core batch path (B > 1), then asks L2 to fetch its
  * share of next's predictor hidden-layer weights (W1, PowerInfer §5.1) once
  * it has issued the copies of its own rows, so that those bytes move while
  * other blocks finish and while the reduction runs; the next predictor then
@@ -278,6 +279,31 @@ sffn_status sffn_layer_set_zero_skip(sffn_layer* layer, int32_t enable, int32_t*
  * Errors: INVALID_ARG (layer NULL, a count outside [0, number of SMs], or
  * too few FFN blocks for the layer's shared-memory ring). */
 sffn_status sffn_layer_set_grid(sffn_layer* layer, int32_t ffn_blocks, int32_t score_blocks);
+
+/* Which arithmetic serves batched calls (B > 1) on this layer. The batch
+ * reads each row of the union of its tokens' active sets once (KAIROX 问题与
+ * 动机: a batch activates the union of its tokens' neurons; PowerInfer §3.2
+ * on batches below 32):
+ *   SFFN_BATCH_TENSOR      every product on the tensor cores (tcgen05.mma over
+ *                          the union rows, activations as 16-bit hi/lo parts);
+ *   SFFN_BATCH_CUDA_CORES  for 2 <= B <= 4: fp32 FFMA on the CUDA cores, the
+ *                          B = 1 kernels' structure with every token's x in
+ *                          registers (16-bit SFFN_FFN_ROWS weights, d <= 8192;
+ *                          otherwise UNSUPPORTED); B > 4 takes the tensor cores;
+ *   SFFN_BATCH_AUTO        the default: the CUDA cores for B = 2 where they
+ *                          apply, the tensor cores otherwise (measured on
+ *                          GB300: the CUDA-core arm is faster at B = 2 and
+ *                          slower from B = 3 on).
+ * Results agree within the parity tolerances either way; both arms write the
+ * same views. Host only. Errors: INVALID_ARG (layer NULL, unknown path). */
+typedef enum { SFFN_BATCH_AUTO = 0, SFFN_BATCH_TENSOR = 1, SFFN_BATCH_CUDA_CORES = 2 } sffn_batch_path;
+sffn_status sffn_layer_set_batch_path(sffn_layer* layer, int32_t path);
+
+/* The arm that serves a batched call of B tokens on this layer under its
+ * current setting: SFFN_BATCH_TENSOR or SFFN_BATCH_CUDA_CORES, or -1 when no
+ * arm does (B outside [2, max_batch], or a layer the batched paths do not
+ * take: such a call returns UNSUPPORTED). Host only. */
+int32_t sffn_layer_batch_arm(const sffn_layer* layer, int32_t B);
 
 /* ---------------------------------------------------------------- hot calls */
 

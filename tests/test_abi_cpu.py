@@ -108,6 +108,13 @@ def test_null_handles_are_rejected_on_the_host(lib):
     assert L.sffn_layer_set_grid(None, 0, 0) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_layer_set_l2_resident(None, None) == lib.SFFN_ERR_INVALID_ARG
     assert L.sffn_layer_set_zero_skip(None, 1, None) == lib.SFFN_ERR_INVALID_ARG
+    assert L.sffn_layer_set_batch_path(None, 0) == lib.SFFN_ERR_INVALID_ARG
+    assert L.sffn_layer_batch_arm(None, 2) == -1
+    assert L.sffn_stack_create(None, 1, ctypes.byref(ctypes.c_void_p())) == lib.SFFN_ERR_INVALID_ARG
+    assert L.sffn_stack_workspace_bytes(None) == 0
+    assert L.sffn_stack_check_error(None, None) == lib.SFFN_ERR_INVALID_ARG
+    assert L.sffn_stack_decode(None, None, None, None, 0.0, ctypes.byref(m), None, 0, None) == lib.SFFN_ERR_INVALID_ARG
+    L.sffn_stack_destroy(None)
     out = ctypes.c_void_p()
     assert L.sffn_layer_create(None, ctypes.byref(out)) == lib.SFFN_ERR_INVALID_ARG
     bad = lib.make_desc(100, 2048, 64, 32, "relu", "f32")

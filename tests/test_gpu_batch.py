@@ -81,7 +81,22 @@ SHAPES = [
 def test_batch_matches_oracle(sffn, d, f, h, G, act, dt, B):
     spec = W.LayerSpec(name="t", d=d, f=f, h=h, group_size=G, act=act, wdtype=dt, p_mean=0.12, zipf_alpha=1.0)
     L, w, host = make_layer(spec, seed=B, max_batch=32, biases=(B == 5))
+    L.set_batch_path("tensor")          # the tensor-core products at every B (auto takes B = 2 to CUDA cores)
     X = W.make_tokens(d, 1, seed=B, batch=B, device="cuda")[0]
+    masks, y, _ = _run(sffn, L, X, 0.0)
+    _check_batch(host, spec, X, 0.0, masks, y)
+    L.check_error()
+
+
+def test_auto_path_at_two_tokens(sffn):
+    """The default choice at B = 2 (the CUDA-core arm on 16-bit rows) against the oracle."""
+    spec = W.LayerSpec(name="t", d=2048, f=4096, h=256, group_size=64, act="reglu", wdtype="bf16", p_mean=0.12,
+                       zipf_alpha=1.0)
+    L, w, host = make_layer(spec, seed=31, max_batch=32)
+    assert sffn.sffn_layer_batch_arm(L.handle, 2) == "cuda_cores"
+    assert sffn.sffn_layer_batch_arm(L.handle, 3) == "tensor"
+    assert sffn.sffn_layer_batch_arm(L.handle, 1) is None
+    X = W.make_tokens(spec.d, 1, seed=32, batch=2, device="cuda")[0]
     masks, y, _ = _run(sffn, L, X, 0.0)
     _check_batch(host, spec, X, 0.0, masks, y)
     L.check_error()
@@ -192,3 +207,71 @@ def test_fp32_batch_is_unsupported(sffn):
     with pytest.raises(sffn.SffnError) as e:
         sffn.sffn_decode_step(L.handle, X, 4, 0.0, L.masks(4), y, None, L.workspace(1))
     assert e.value.status == sffn.SFFN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ the CUDA-core arm (2 <= B <= 4)
+
+CC_SHAPES = [s for s in SHAPES] + [(8192, 4096, 1024, 64, "reglu", "bf16"), (4096, 11008, 512, 32, "swiglu", "bf16")]
+
+
+@pytest.mark.parametrize("d,f,h,G,act,dt", CC_SHAPES)
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_cuda_core_arm_matches_oracle(sffn, d, f, h, G, act, dt, B):
+    spec = W.LayerSpec(name="t", d=d, f=f, h=h, group_size=G, act=act, wdtype=dt, p_mean=0.12, zipf_alpha=1.0)
+    L, w, host = make_layer(spec, seed=40 + B, max_batch=32, biases=(B == 3))
+    L.set_batch_path("cuda_cores")
+    X = W.make_tokens(d, 1, seed=B, batch=B, device="cuda")[0]
+    masks, y, xo = _run(sffn, L, X, 0.0, x_out=True)
+    _check_batch(host, spec, X, 0.0, masks, y)
+    assert torch.equal(xo, X + y)
+    L.check_error()
+
+
+def test_cuda_core_arm_forward_and_predict_views(sffn):
+    """Caller masks through sffn_forward (the union formed from them) and
+    sffn_predict's views, on the CUDA-core arm; B = 5 falls to the tensor cores."""
+    spec = W.LayerSpec(name="t", d=1024, f=2048, h=128, group_size=32, act="relu", wdtype="bf16", p_mean=0.1,
+                       zipf_alpha=1.0)
+    L, w, host = make_layer(spec, seed=12, max_batch=32)
+    L.set_batch_path("cuda_cores")
+    B = 4
+    rng = np.random.default_rng(13)
+    bits = rng.random((B, spec.f)) < np.array([0.0, 1.0, 0.01, 0.3])[:, None]
+    masks = L.masks(B)
+    masks.nmask.copy_(torch.from_numpy(np.stack([O.bits_to_words(b).view(np.int32) for b in bits])).cuda())
+    X = W.make_tokens(spec.d, 1, seed=14, batch=B, device="cuda")[0]
+    y = torch.empty(B, spec.d, device="cuda")
+    sffn.sffn_forward(L.handle, X, B, masks, y, None, L.workspace(B))
+    torch.cuda.synchronize()
+    for b in range(B):
+        check_y(y[b].cpu().numpy(), host.ffn(X[b].double().cpu().numpy(), bits[b], "relu"), "bf16", f"y[{b}]")
+    assert (y[0] == 0).all()
+    union = bits.any(axis=0)
+    assert masks.ucount.item() == int(union.sum())
+    assert np.array_equal(words_bits(masks.unmask.cpu().numpy(), spec.f), union)
+    m1 = L.masks(B)
+    sffn.sffn_predict(L.handle, X, B, 0.0, m1, L.workspace(B))
+    m2, y2, _ = _run(sffn, L, X, 0.0)
+    for k in ("nmask", "gmask", "count", "unmask", "ugmask", "ucount"):
+        assert torch.equal(getattr(m1, k), getattr(m2, k)), k
+    X5 = W.make_tokens(spec.d, 1, seed=15, batch=5, device="cuda")[0]
+    m5, y5, _ = _run(sffn, L, X5, 0.0)
+    _check_batch(host, spec, X5, 0.0, m5, y5)
+    L.check_error()
+
+
+def test_cuda_core_arm_full_size_falcon(sffn):
+    spec = W.WORKLOADS["falcon40b_relu_d8192_f32768_fp16_batch"]
+    L, w, host = make_layer(spec, seed=0, max_batch=32)
+    L.set_batch_path("cuda_cores")
+    B = 4
+    X = W.make_tokens(spec.d, 1, seed=0, batch=B, device="cuda")[0]
+    masks, y, _ = _run(sffn, L, X, spec.thres)
+    for b in range(B):
+        xs = X[b].double().cpu().numpy()
+        check_masks(host.scores(xs), spec.thres, spec.group_size, masks.nmask[b].cpu().numpy(),
+                    masks.gmask[b].cpu().numpy(), masks.idx[b].cpu().numpy(), masks.count[b].item())
+        if b in (0, B - 1):
+            gb = words_bits(masks.nmask[b].cpu().numpy(), spec.f)
+            check_y(y[b].cpu().numpy(), host.ffn(xs, gb, spec.act), spec.wdtype, f"y[{b}]")
+    L.check_error()
