@@ -53,8 +53,6 @@ struct GemmArgs {
   size_t dmat_stride;       // floats from the first matrix's partials to the second's
   int grid;                 // CTAs launched
   uint32_t* err;
-  const unsigned char* pf;  // L2 hint: bytes this product's CTAs prefetch once their copies are issued (or null)
-  size_t pf_bytes;
 };
 
 // Work decomposition shared by the GEMM and its finishers (stream-K): the
@@ -297,13 +295,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   producers_done:
-    // L2 hint: this CTA's share of the next layer's hidden-layer weights,
-    // requested once its own copies are issued (null without a hint)
-    if (tid == 0 && g.pf && !*(volatile int*)&s_abort) {
-      const size_t units = g.pf_bytes / 16;
-      const size_t lo = units * blockIdx.x / gridDim.x * 16, hi = units * (blockIdx.x + 1) / gridDim.x * 16;
-      for (size_t o = lo; o < hi; o += 65536) prefetch_l2_bulk(g.pf + o, (uint32_t)min(hi - o, (size_t)65536));
-    }
     if (GATHER) tc::cp_async_wait_all();
     // let this CTA's TMA loads that no MMA consumed land before exiting
     if (tid == 0 && *(volatile int*)&s_abort) {
@@ -1003,10 +994,6 @@ cudaError_t launch_batch(const sffn_layer& L, const float* x, int B, float thres
   dn.D = reinterpret_cast<float*>(base + w.dy);
   dn.grid = grid;
   dn.err = L.err;
-  if (L.next) {  // sffn_layer_set_next: the next layer's W1 into L2 during the down product's tail
-    dn.pf = static_cast<const unsigned char*>(L.next->W1);
-    dn.pf_bytes = (size_t)L.next->desc.h * L.next->desc.d * L.next->wbytes;
-  }
   e = encode_rows(&dn.tmB, hhl, bf, fpad, 2 * npad, 2 * npad);
   if (e == cudaSuccess) e = traced_b(L, 3, st, [&] { return launch_down(L, npad, dn, st); });
   if (e != cudaSuccess) return e;

@@ -117,7 +117,8 @@ __device__ __forceinline__ void cc_transpose_reduce32(float (&v)[32], int lane) 
 }
 
 // Persistent blocks over contiguous ranges of mask words, W2 rows of one word
-// per ring stage; the tokens are taken one after another over the stage.
+// per ring stage; every token's 32 sums of a stage are formed in one pass over
+// the stage (each weight chunk read from shared memory once for all tokens).
 template <typename T, int NB>
 __global__ void __launch_bounds__(kCcScoreThreads, 1)
     k_cc_scores(const T* __restrict__ W2, const float* __restrict__ b2, const float* hid, int B, float thres,
@@ -132,8 +133,7 @@ __global__ void __launch_bounds__(kCcScoreThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   float* s_hid = reinterpret_cast<float*>(smem + (size_t)stages * word_bytes);  // [NB][h]
   uint64_t* full = reinterpret_cast<uint64_t*>(s_hid + (size_t)NB * h);
-  __shared__ float red[kCcScoreThreads / 32][32];
-  __shared__ uint32_t s_word[NB];
+  __shared__ float red[NB][kCcScoreThreads / 32][32];
   __shared__ int s_issued;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(kCcScoreThreads, 1)
   }
   pdl_launch_dependents();
   pdl_wait();
-  for (int i = threadIdx.x * 4; i < B * h; i += kCcScoreThreads * 4)
-    *reinterpret_cast<float4*>(s_hid + i) = ld_dep4(hid + i);
+  for (int i = threadIdx.x * 4; i < NB * h; i += kCcScoreThreads * 4)
+    *reinterpret_cast<float4*>(s_hid + i) = i < B * h ? ld_dep4(hid + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nch = h / EPC;
@@ -166,47 +166,58 @@ __global__ void __launch_bounds__(kCcScoreThreads, 1)
     const int s = k % stages;
     const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / stages) & 1));
     const unsigned char* sp = smem + (size_t)s * word_bytes;
-    for (int b = 0; b < B; ++b) {
-      float acc[32];
+    float acc[NB][32];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) acc[r] = 0.f;
-      const float* hb = s_hid + (size_t)b * h;
-      for (int c = c0 + lane; c < c1; c += 32) {
-        float hv[EPC];
+    for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) hv[e] = hb[c * EPC + e];
+      for (int r = 0; r < 32; ++r) acc[b][r] = 0.f;
+    for (int c = c0 + lane; c < c1; c += 32) {
+      float hv[NB][EPC];
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          acc[r] += dot_chunk<T>(*reinterpret_cast<const uint4*>(sp + (size_t)r * row_bytes + (size_t)c * 16), hv);
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) hv[b][e] = s_hid[(size_t)b * h + c * EPC + e];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        float w[EPC];
+        WType<T>::unpack(*reinterpret_cast<const uint4*>(sp + (size_t)r * row_bytes + (size_t)c * 16), w);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float t = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) t = fmaf(w[e], hv[b][e], t);
+          acc[b][r] += t;
+        }
       }
-      cc_transpose_reduce32(acc, lane);
-      red[warp][lane] = acc[0];
-      __syncthreads();
-      if (warp == 0) {
-        float sc = red[0][lane];
+    }
 #pragma unroll
-        for (int w2 = 1; w2 < kCcScoreThreads / 32; ++w2) sc += red[w2][lane];
-        if (b2) sc += b2[(size_t)(w0 + k) * 32 + lane];
-        const uint32_t m = __ballot_sync(SFFN_FULL_MASK, sc >= thres);  // NaN compares false
-        if (lane == 0) s_word[b] = m;
-      }
-      __syncthreads();
+    for (int b = 0; b < NB; ++b) {
+      cc_transpose_reduce32(acc[b], lane);
+      red[b][warp][lane] = acc[b][0];
     }
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
     }
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
       uint32_t u = 0;
+      const float bias = b2 ? b2[(size_t)(w0 + k) * 32 + lane] : 0.f;
       for (int b = 0; b < B; ++b) {
-        nmask[(size_t)b * nw + w0 + k] = s_word[b];
-        u |= s_word[b];
+        float sc = red[b][0][lane];
+#pragma unroll
+        for (int w2 = 1; w2 < kCcScoreThreads / 32; ++w2) sc += red[b][w2][lane];
+        if (b2) sc += bias;
+        const uint32_t m = __ballot_sync(SFFN_FULL_MASK, sc >= thres);  // NaN compares false
+        if (lane == 0) nmask[(size_t)b * nw + w0 + k] = m;
+        u |= m;
       }
-      unmask[w0 + k] = u;
-      if (k + stages < nloc) {
-        fence_proxy_async_smem();
-        issue(k + stages);
-        s_issued = k + stages + 1;
+      if (lane == 0) {
+        unmask[w0 + k] = u;
+        if (k + stages < nloc) {
+          fence_proxy_async_smem();
+          issue(k + stages);
+          s_issued = k + stages + 1;
+        }
       }
     }
     __syncthreads();

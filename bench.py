@@ -423,7 +423,7 @@ def run_ours(args, world, rank, local):
         cc_arm = sffn.sffn_layer_batch_arm(layers[0].handle, Bt) == "cuda_cores"
     # L2 hint: each layer's FFN kernel warms the next layer's predictor weights
     # (the last layer warms layer 0 for the next token)
-    prefetch_next = not args.no_prefetch_next
+    prefetch_next = Bt == 1 and not args.no_prefetch_next
     # actual-activation zero-skip: each layer reports the downT rows it read
     zero_skip = bool(args.zero_skip)
     if zero_skip and Bt != 1:

@@ -218,11 +218,10 @@ typedef struct {
 
 sffn_status sffn_layer_set_trace(sffn_layer* layer, const sffn_trace* trace /* host, or NULL */);
 
-/* Optional L2 hint for a layer stack. `next` names the layer whose
+/* Optional L2 hint for a layer stack at B = 1. `next` names the layer whose
  * hot call follows this layer's on the same stream (in a stack: layer l + 1,
  * and for the last layer layer 0 of the next token), or NULL to turn the hint
- * off. Each block of this layer's sparse-FFN kernel (B = 1), or of its down
- * product on the tensor-core batch path (B > 1), then asks L2 to fetch its
+ * off. Each block of this layer's sparse-FFN kernel then asks L2 to fetch its
  * share of next's predictor hidden-layer weights (W1, PowerInfer §5.1) once
  * it has issued the copies of its own rows, so that those bytes move while
  * other blocks finish and while the reduction runs; the next predictor then
