@@ -375,3 +375,59 @@ def test_l2_resident_from_momentum_matches_oracle(sffn):
     for L, _, _ in built:
         L.set_l2_resident(None)
         L.check_error()
+
+
+# ------------------------------------------------------------------ the largest layers the library accepts
+
+def test_maximum_row_length_and_group_count(sffn):
+    """d = 16384 with 16-bit weights (32 KB rows, the longest accepted) at B = 1;
+    f = 65536 in 1024 groups of 64 (the most groups, 2048 mask words: the
+    longest scan) at B = 1 and through the tensor-core batch path at B = 32;
+    and a momentum step over all 1024 groups. Masks and y against the oracle."""
+    spec = W.LayerSpec(name="t", d=16384, f=2048, h=256, group_size=32, act="relu", wdtype="bf16", p_mean=0.15,
+                       zipf_alpha=1.0)
+    L, w, host = make_layer(spec, seed=51)
+    X = W.make_tokens(spec.d, 2, seed=52, device="cuda")
+    for t in range(X.shape[0]):
+        masks, y, _ = _decode(sffn, L, X[t], 0.0)
+        _check_token(host, spec, X[t], 0.0, masks, y)
+    L.check_error()
+    del L, w, host
+
+    spec = W.LayerSpec(name="t", d=1024, f=65536, h=128, group_size=64, act="reglu", wdtype="f16", p_mean=0.05,
+                       zipf_alpha=1.0)
+    L, w, host = make_layer(spec, seed=53, max_batch=32)
+    X = W.make_tokens(spec.d, 2, seed=54, device="cuda")
+    for t in range(X.shape[0]):
+        masks, y, _ = _decode(sffn, L, X[t], 0.0)
+        _check_token(host, spec, X[t], 0.0, masks, y)
+    B = 32
+    XB = W.make_tokens(spec.d, 1, seed=55, batch=B, device="cuda")[0]
+    mb, wsb = L.masks(B), L.workspace(B)
+    yb = torch.full((B, spec.d), float("nan"), device="cuda")
+    sffn.sffn_decode_step(L.handle, XB, B, 0.0, mb, yb, None, wsb)
+    torch.cuda.synchronize()
+    union = np.zeros(spec.f, dtype=bool)
+    for b in range(B):
+        xs = XB[b].double().cpu().numpy()
+        check_masks(host.scores(xs), 0.0, spec.group_size, mb.nmask[b].cpu().numpy(), mb.gmask[b].cpu().numpy(),
+                    mb.idx[b].cpu().numpy(), mb.count[b].item())
+        gb = words_bits(mb.nmask[b].cpu().numpy(), spec.f)
+        union |= gb
+        if b in (0, B - 1):
+            check_y(yb[b].cpu().numpy(), host.ffn(xs, gb, spec.act), spec.wdtype, f"y[{b}]")
+    assert mb.ucount.item() == int(union.sum())
+    # the momentum step over all 1024 groups, fed the union group mask
+    ng = spec.n_groups
+    tam = sffn.Tam(1, ng, 0.9)
+    outs = sffn.TamOutputs(1, ng, 512)
+    s_ref, prev = np.zeros(ng, dtype=np.float32), np.zeros(ng, dtype=bool)
+    for _ in range(3):
+        sffn.tam_update(tam.handle, 0, 1, mb.ugmask, (ng + 31) // 32, -1.0, 0.01, 512, outs)
+        r = O.tam_update(s_ref, prev, words_bits(mb.ugmask.cpu().numpy(), ng), np.float32(0.9), np.float32(0.01), 512)
+        s_ref, prev = r["scores"], r["resident"]
+        k = r["topk"].shape[0]
+        assert np.array_equal(outs.topk[0, :k].cpu().numpy(), r["topk"])
+        assert np.array_equal(words_bits(outs.resident[0].cpu().numpy(), ng), r["resident"])
+    L.check_error()
+    sffn.tam_check_error(tam.handle)
