@@ -28,6 +28,7 @@ namespace {
 constexpr int kCcHidRows = 4;
 constexpr int kCcHidThreads = 256;
 constexpr int kCcScoreThreads = 128;
+constexpr int kCcScorePreStages = 2;                // W2 ring stages requested before the dependency wait
 constexpr int kCcWarps = 8;                       // FFN consumer warps
 constexpr int kCcConsumers = kCcWarps * 32;
 constexpr int kCcThreads = kCcConsumers + 32;     // + producer warp
@@ -146,13 +147,19 @@ __global__ void __launch_bounds__(kCcScoreThreads, 1)
     mbar_arrive_expect_tx(&full[s], word_bytes);
     bulk_g2s(smem + (size_t)s * word_bytes, W2 + (size_t)(w0 + k) * 32 * h, word_bytes, &full[s], pol);
   };
+  // at most kCcScorePreStages stages before the wait, the rest of the ring
+  // right after it (as in the B = 1 scores kernel: a larger early burst
+  // delays the wait's return)
+  const int first = min(stages, nloc);
+  const int pre = min(first, kCcScorePreStages);
   if (threadIdx.x == 0) {
-    const int first = min(stages, nloc);
-    for (int k = 0; k < first; ++k) issue(k);
+    for (int k = 0; k < pre; ++k) issue(k);
     s_issued = first;
   }
   pdl_launch_dependents();
   pdl_wait();
+  if (threadIdx.x == 0)
+    for (int k = pre; k < first; ++k) issue(k);
   for (int i = threadIdx.x * 4; i < NB * h; i += kCcScoreThreads * 4)
     *reinterpret_cast<float4*>(s_hid + i) = i < B * h ? ld_dep4(hid + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
