@@ -388,6 +388,9 @@ __global__ void __launch_bounds__(kReduceThreads)
   const int cg = threadIdx.x % CG, pg = threadIdx.x / CG;
   const int col = blockIdx.x * kReduceCols + cg * 4;
   __shared__ float4 red[GROUPS][CG];
+  // the residual's x, requested together with the partials (one round trip)
+  const bool adds = threadIdx.x < CG && col < d;
+  const float4 xv = (x_out && adds) ? ld_dep4(x + col) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 v[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(kReduceThreads)
   }
   red[pg][cg] = acc;
   __syncthreads();
-  if (threadIdx.x < CG && col < d) {
+  if (adds) {
     float4 sum = red[0][cg];
 #pragma unroll
     for (int g = 1; g < GROUPS; ++g) {
@@ -409,10 +412,8 @@ __global__ void __launch_bounds__(kReduceThreads)
       sum.x += w.x; sum.y += w.y; sum.z += w.z; sum.w += w.w;
     }
     *reinterpret_cast<float4*>(y + col) = sum;
-    if (x_out) {
-      const float4 xv = ld_dep4(x + col);
+    if (x_out)
       *reinterpret_cast<float4*>(x_out + col) = make_float4(xv.x + sum.x, xv.y + sum.y, xv.z + sum.z, xv.w + sum.w);
-    }
   }
   // zero-skip: the downT rows the FFN blocks read (one warp of the last block;
   // an integer sum, so its order does not matter)
