@@ -87,7 +87,10 @@ def parse_args():
                    help="workloads with a topic shift: keep one topic (by default the second half of the cycled "
                         "tokens runs with every layer's group ranks redrawn)")
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
-    return p.parse_args()
+    args = p.parse_args()
+    if args.profile_steps < 1:
+        p.error("--profile-steps must be at least 1: the roofline line comes from the traced pass")
+    return args
 
 
 def dist_env():
