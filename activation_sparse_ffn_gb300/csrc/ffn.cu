@@ -426,6 +426,15 @@ __global__ void __launch_bounds__(kReduceThreads)
   }
 }
 
+// Largest chunk count per consumer thread a row of type T can need: rows are
+// at most 32 KB of 16- or 32-bit weights (8 chunks per thread), so at most
+// 16 KB of 8-bit codes (4) and 8 KB of 4-bit codes (2). Only these
+// instantiations are built.
+template <typename T>
+constexpr int max_ffn_cpt() {
+  return std::is_same<T, q4x2_t>::value ? 2 : std::is_same<T, int8_t>::value ? 4 : 8;
+}
+
 template <typename T, int ACT>
 cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, cudaStream_t st, const float* x,
                          const uint32_t* nmask, int list_cap, int32_t* idx_out, int32_t* count_out,
@@ -446,8 +455,12 @@ cudaError_t launch_ffn_t(const sffn_layer& L, int cpt, dim3 grid, size_t smem, c
   switch (cpt) {
     case 1: return launch_ex(k_ffn<T, ACT, 1>, SFFN_FFN_ARGS);
     case 2: return launch_ex(k_ffn<T, ACT, 2>, SFFN_FFN_ARGS);
-    case 4: return launch_ex(k_ffn<T, ACT, 4>, SFFN_FFN_ARGS);
-    default: return launch_ex(k_ffn<T, ACT, 8>, SFFN_FFN_ARGS);
+    case 4:
+      if constexpr (max_ffn_cpt<T>() >= 4) return launch_ex(k_ffn<T, ACT, 4>, SFFN_FFN_ARGS);
+      return cudaErrorInvalidConfiguration;
+    default:
+      if constexpr (max_ffn_cpt<T>() >= 8) return launch_ex(k_ffn<T, ACT, 8>, SFFN_FFN_ARGS);
+      return cudaErrorInvalidConfiguration;
   }
 #undef SFFN_FFN_ARGS
 }
@@ -464,8 +477,10 @@ cudaError_t set_ffn_attr(size_t smem) {
   cudaError_t e;
   if ((e = set_big_smem(k_ffn<T, ACT, 1>, smem))) return e;
   if ((e = set_big_smem(k_ffn<T, ACT, 2>, smem))) return e;
-  if ((e = set_big_smem(k_ffn<T, ACT, 4>, smem))) return e;
-  return set_big_smem(k_ffn<T, ACT, 8>, smem);
+  if constexpr (max_ffn_cpt<T>() >= 4)
+    if ((e = set_big_smem(k_ffn<T, ACT, 4>, smem))) return e;
+  if constexpr (max_ffn_cpt<T>() >= 8) return set_big_smem(k_ffn<T, ACT, 8>, smem);
+  return cudaSuccess;
 }
 
 int ffn_cpt(const sffn_layer& L) {
