@@ -351,10 +351,12 @@ def stack_layers(spec, args) -> tuple[object, str | None]:
 
 
 def rms_normalize(x):
-    """x / rms(x) over the last axis (no learned scale): the harness stand-in
-    for the normalisation a transformer block applies before its FFN."""
-    import torch
-    return x * torch.rsqrt((x * x).mean(dim=-1, keepdim=True))
+    """x / rms(x) over the last axis (no learned scale, no epsilon): the
+    harness stand-in for the normalisation a transformer block applies before
+    its FFN. PyTorch's fused rms_norm: half the cost of the same expression
+    spelled out in elementwise ops."""
+    import torch.nn.functional as F
+    return F.rms_norm(x, (x.shape[-1],), eps=0.0)
 
 
 def percentiles_ms(durs: list[float]) -> dict:
