@@ -141,3 +141,22 @@ def test_clock_summary_uses_busy_samples_and_names_throttle_reasons(tmp_path):
 def test_clock_summary_without_nvidia_smi():
     out = bench.ClockSampler(0).stop()
     assert out["samples"] == 0 and out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_normalize_stand_in_is_x_over_rms():
+    """The --normalize harness op divides by the root mean square with no
+    epsilon and no learned scale (reading R24), whatever routine computes it."""
+    import torch
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(3, 4096, generator=g, dtype=torch.float64) * torch.tensor([[1e-3], [1.0], [1e3]], dtype=torch.float64)
+    rms = torch.sqrt((x * x).mean(dim=-1, keepdim=True))
+    assert torch.allclose(bench.rms_normalize(x), x / rms, rtol=1e-12, atol=0)
+
+
+def test_profile_steps_must_be_positive(monkeypatch):
+    """The roofline line comes from the traced pass, so zero traced steps is refused up front."""
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--profile-steps", "0"])
+    with pytest.raises(SystemExit):
+        bench.parse_args()
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--profile-steps", "1"])
+    assert bench.parse_args().profile_steps == 1
